@@ -1,0 +1,220 @@
+"""PyTorch-facing binding of liblp.so.
+
+Argument marshalling only: every op passes device pointers, sizes, strides and
+the current CUDA stream to the C entry point of the same name (include/lp.h),
+which does all of the work in its own kernels.  PyTorch supplies device memory
+and streams.  The names follow the pages: ``apply_token_bitmask_inplace``
+(XGrammar "Bitmask Operations"), ``apply_packed_bitmask`` (Modular MAX), and
+``sample`` (Kernel Hub "logits-processor"); ``lp_*`` aliases carry the C names.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Sequence
+
+import torch
+
+from . import _lib
+from ._lib import SamplingParams, check
+
+_DT = {torch.float32: _lib.LP_F32, torch.float16: _lib.LP_F16, torch.bfloat16: _lib.LP_BF16}
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    try:
+        return _DT[t.dtype]
+    except KeyError:
+        raise TypeError(f"logits must be float32, float16 or bfloat16, not {t.dtype}") from None
+
+
+def _matrix(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dim() == 1:
+        t = t.unsqueeze(0)
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 1-D or 2-D, got {tuple(t.shape)}")
+    if t.size(1) > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} rows must be contiguous (stride(1) == 1)")
+    return t
+
+
+def _stream(t: torch.Tensor):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _bitmask(bitmask: torch.Tensor, device) -> torch.Tensor:
+    bm = _matrix(bitmask, "bitmask")
+    if bm.dtype != torch.int32:
+        raise TypeError("bitmask must be int32")
+    if bm.device != device:
+        raise ValueError("bitmask must be on the same device as logits")
+    return bm
+
+
+def _indices(indices, device):
+    if indices is None:
+        return None
+    if isinstance(indices, torch.Tensor):
+        idx = indices.to(device=device, dtype=torch.int32).contiguous()
+    else:
+        idx = torch.tensor(list(indices), dtype=torch.int32, device=device)
+    return idx
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stride(t: torch.Tensor) -> int:
+    return t.stride(0) if t.size(0) > 1 or t.size(1) <= 1 else max(t.stride(0), t.size(1))
+
+
+def apply_token_bitmask_inplace(logits: torch.Tensor, bitmask: torch.Tensor, *,
+                                vocab_size: int | None = None,
+                                indices: Sequence[int] | torch.Tensor | None = None) -> None:
+    """Set masked logits to -inf in place (bit 0 = masked, bit 1 = kept)."""
+    lg = _matrix(logits, "logits")
+    bm = _bitmask(bitmask, lg.device)
+    idx = _indices(indices, lg.device)
+    lib = _lib.load()
+    st = lib.lp_apply_token_bitmask(
+        _ptr(lg), _dtype_code(lg), lg.size(0), lg.size(1), _stride(lg), _ptr(bm), bm.size(0),
+        bm.size(1), _stride(bm), -1 if vocab_size is None else int(vocab_size), _ptr(idx),
+        0 if idx is None else idx.numel(), _stream(lg))
+    check("lp_apply_token_bitmask", st)
+
+
+lp_apply_token_bitmask = apply_token_bitmask_inplace
+
+
+def apply_packed_bitmask(logits: torch.Tensor, bitmask: torch.Tensor,
+                         fill_value: float = float("-inf"), *, out: torch.Tensor | None = None,
+                         vocab_size: int | None = None,
+                         indices: Sequence[int] | torch.Tensor | None = None) -> torch.Tensor:
+    """Out-of-place apply: masked positions take ``fill_value``; returns ``out``."""
+    lg = _matrix(logits, "logits")
+    bm = _bitmask(bitmask, lg.device)
+    if out is None:
+        out = torch.empty_like(lg)
+    o = _matrix(out, "out")
+    if o.dtype != lg.dtype or o.shape != lg.shape:
+        raise ValueError("out must match logits in dtype and shape")
+    idx = _indices(indices, lg.device)
+    lib = _lib.load()
+    st = lib.lp_apply_packed_bitmask(
+        _ptr(o), _stride(o), _ptr(lg), _dtype_code(lg), lg.size(0), lg.size(1), _stride(lg),
+        _ptr(bm), bm.size(0), bm.size(1), _stride(bm), float(fill_value),
+        -1 if vocab_size is None else int(vocab_size), _ptr(idx),
+        0 if idx is None else idx.numel(), _stream(lg))
+    check("lp_apply_packed_bitmask", st)
+    return out
+
+
+lp_apply_packed_bitmask = apply_packed_bitmask
+
+
+def _param(v, B, dtype, device, keep):
+    """A per-row parameter: (device pointer or None, scalar)."""
+    if isinstance(v, torch.Tensor) and v.numel() != 1:
+        if v.numel() != B:
+            raise ValueError(f"per-row parameter must have {B} values, got {v.numel()}")
+        t = v.to(device=device, dtype=dtype).contiguous()
+        keep.append(t)
+        return ctypes.c_void_p(t.data_ptr()), 0
+    s = v.item() if isinstance(v, torch.Tensor) else v
+    return None, (int(s) if dtype == torch.int32 else float(s))
+
+
+def _params(B, device, temperature, top_k, top_p, min_p, seed, offset, keep):
+    p = SamplingParams()
+    p.temperature, p.temperature_scalar = _param(temperature, B, torch.float32, device, keep)
+    p.top_k, p.top_k_scalar = _param(top_k, B, torch.int32, device, keep)
+    p.top_p, p.top_p_scalar = _param(top_p, B, torch.float32, device, keep)
+    p.min_p, p.min_p_scalar = _param(min_p, B, torch.float32, device, keep)
+    p.seed = int(seed) & (2**64 - 1)
+    p.offset = int(offset) & (2**64 - 1)
+    return p
+
+
+def _ids_out(out, B, device):
+    if out is None:
+        return torch.empty(B, dtype=torch.int64, device=device)
+    if out.dtype != torch.int64 or out.numel() != B or not out.is_contiguous():
+        raise ValueError("out must be a contiguous int64 tensor of B elements")
+    return out
+
+
+def sample(logits: torch.Tensor, temperature=1.0, top_k=0, top_p=1.0, min_p=0.0, seed: int = 0,
+           offset: int = 0, *, vocab_size: int | None = None,
+           out: torch.Tensor | None = None) -> torch.Tensor:
+    """Temperature, top-k ∩ top-p ∩ min-p, Gumbel-max draw keyed by
+    (seed, row, offset); greedy for temperature <= 0 or top_k == 1.  Every
+    parameter is a scalar or a length-B tensor.  Returns int64 ids [B]."""
+    lg = _matrix(logits, "logits")
+    B = lg.size(0)
+    keep: list = []
+    p = _params(B, lg.device, temperature, top_k, top_p, min_p, seed, offset, keep)
+    ids = _ids_out(out, B, lg.device)
+    lib = _lib.load()
+    st = lib.lp_sample(_ptr(lg), _dtype_code(lg), B,
+                       lg.size(1) if vocab_size is None else int(vocab_size), _stride(lg),
+                       ctypes.byref(p), _ptr(ids), _stream(lg))
+    check("lp_sample", st)
+    return ids
+
+
+lp_sample = sample
+
+
+def mask_and_sample(logits: torch.Tensor, bitmask: torch.Tensor | None, temperature=1.0,
+                    top_k=0, top_p=1.0, min_p=0.0, seed: int = 0, offset: int = 0, *,
+                    indices: Sequence[int] | torch.Tensor | None = None,
+                    vocab_size: int | None = None,
+                    out: torch.Tensor | None = None) -> torch.Tensor:
+    """The bitmask applied on the fly (logits are not written), then ``sample``.
+    Rows in ``indices`` (all rows when None) are masked; a masked row whose mask
+    admits no token returns -1."""
+    lg = _matrix(logits, "logits")
+    B = lg.size(0)
+    bm = None if bitmask is None else _bitmask(bitmask, lg.device)
+    idx = _indices(indices, lg.device)
+    keep: list = []
+    p = _params(B, lg.device, temperature, top_k, top_p, min_p, seed, offset, keep)
+    ids = _ids_out(out, B, lg.device)
+    lib = _lib.load()
+    st = lib.lp_mask_and_sample(
+        _ptr(lg), _dtype_code(lg), B, lg.size(1), _stride(lg), _ptr(bm),
+        0 if bm is None else bm.size(0), 0 if bm is None else bm.size(1),
+        0 if bm is None else _stride(bm), -1 if vocab_size is None else int(vocab_size),
+        _ptr(idx), 0 if idx is None else idx.numel(), ctypes.byref(p), _ptr(ids), _stream(lg))
+    check("lp_mask_and_sample", st)
+    return ids
+
+
+lp_mask_and_sample = mask_and_sample
+
+
+def philox4x32_10(counters: torch.Tensor, keys: torch.Tensor) -> torch.Tensor:
+    """Device Philox4x32-10 on n blocks: counters [n, 4], keys [n, 2] (int32 bit
+    patterns on the GPU) -> [n, 4] words (int32 bit patterns)."""
+    c = counters.to(torch.int32).contiguous()
+    k = keys.to(torch.int32).contiguous()
+    if c.dim() != 2 or c.size(1) != 4 or k.shape != (c.size(0), 2) or not c.is_cuda:
+        raise ValueError("counters must be [n, 4] and keys [n, 2], on the GPU")
+    out = torch.empty_like(c)
+    lib = _lib.load()
+    check("lp_philox4x32_10",
+          lib.lp_philox4x32_10(_ptr(c), _ptr(k), _ptr(out), c.size(0), _stream(c)))
+    return out
+
+
+lp_philox4x32_10 = philox4x32_10
+
+
+def get_bitmask_shape(batch_size: int, vocab_size: int) -> tuple[int, int]:
+    """(batch_size, ceil(vocab_size / 32)), the packed int32 bitmask shape."""
+    return batch_size, (vocab_size + 31) // 32
+
+
+bitmask_dtype = torch.int32

@@ -1,0 +1,181 @@
+/*
+ * lp.h -- C ABI of liblp.so: grammar-constrained logit masking and fused
+ * per-row sampling on one GB300 GPU (sm_103a).
+ *
+ * Operations (each entry point cites the page section that defines it):
+ *   lp_apply_token_bitmask   in place, masked logits := -inf
+ *   lp_apply_packed_bitmask  out of place, masked logits := fill_value
+ *   lp_sample                temperature, top-k ∩ top-p ∩ min-p, Gumbel-max draw
+ *   lp_mask_and_sample       the bitmask applied on the fly, then lp_sample
+ *
+ * Common conventions
+ *   - Logits are a row-major [B, cols] matrix of float32, float16 or bfloat16 with
+ *     a row stride in ELEMENTS (stride >= cols).  Only the first vocab_size
+ *     columns of a row take part; columns vocab_size..cols-1 are never written.
+ *   - The bitmask is a row-major int32 matrix [bitmask_rows, bitmask_words] with a
+ *     row stride in WORDS.  Token j of row i is bit (j % 32) of word j / 32, the
+ *     word read as an unsigned 32-bit pattern: 1 keeps the token, 0 masks it.
+ *     Bits of tokens >= vocab_size are never used.
+ *   - vocab_size < 0 selects the default min(cols, bitmask_words * 32).
+ *   - indices (optional, int32, device memory): the rows to mask.  The same index
+ *     addresses the logits row and the bitmask row.  NULL masks every row
+ *     (then bitmask_rows >= B is required).  An index outside
+ *     [0, min(B, bitmask_rows)) is skipped on the device: no access, no write.
+ *     Indices should be unique; a duplicate gives the same result as one entry.
+ *   - Pointers are DEVICE pointers unless stated otherwise.  The caller owns every
+ *     buffer.  The library allocates no memory, keeps no state between calls,
+ *     never synchronises, and only enqueues work on the given stream; a call is
+ *     safe from several host threads at once on different buffers.
+ *   - Errors: arguments are checked on the host before any launch.  An invalid
+ *     argument returns LP_ERR_INVALID_ARGUMENT and launches nothing.  A zero-size
+ *     problem returns LP_OK and launches nothing.  A launch failure returns
+ *     LP_ERR_CUDA (the CUDA error is left for cudaGetLastError to report).
+ */
+#ifndef LP_H_
+#define LP_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { LP_F32 = 0, LP_F16 = 1, LP_BF16 = 2 } lp_dtype;
+
+typedef enum {
+  LP_OK = 0,
+  LP_ERR_INVALID_ARGUMENT = 1,
+  LP_ERR_UNSUPPORTED_DTYPE = 2,
+  LP_ERR_CUDA = 3,
+  LP_ERR_TOO_LARGE = 4 /* a row longer than the sampler supports (see lp_sample) */
+} lp_status;
+
+/*
+ * Per-row sampling parameters (Kernel Hub "logits-processor", Ops: every sampling
+ * parameter is a scalar broadcast to all rows or a length-B tensor).  The struct
+ * itself is HOST memory, read during the call.  Each array pointer is a device
+ * pointer to B values, or NULL to use the scalar beside it.
+ *   temperature <= 0 (or NaN)  greedy argmax; else logits are divided by it
+ *   top_k <= 0                 top-k off; top_k == 1 is greedy
+ *   top_p >= 1                 top-p off
+ *   min_p <= 0                 min-p off
+ *   seed, offset               key of the counter-based draw, with the row index
+ */
+typedef struct {
+  const float* temperature;
+  float temperature_scalar;
+  const int32_t* top_k;
+  int32_t top_k_scalar;
+  const float* top_p;
+  float top_p_scalar;
+  const float* min_p;
+  float min_p_scalar;
+  uint64_t seed;
+  uint64_t offset;
+} lp_sampling_params;
+
+/*
+ * lp_apply_token_bitmask -- XGrammar "Bitmask Operations",
+ * apply_token_bitmask_inplace (the row/token loop; Padding and Indices notes);
+ * Kernel Hub "logits-processor", Ops, apply_token_bitmask.
+ *
+ * For each selected row b and each token j < vocab_size whose bit is 0:
+ * logits[b * logits_stride + j] = -inf.  Nothing else changes.
+ *   logits         device, [B, cols] with row stride logits_stride (elements)
+ *   dt             element type of logits
+ *   bitmask        device int32 [bitmask_rows, bitmask_words], stride in words
+ * Invalid: B < 0, cols < 0, logits_stride < cols, bitmask_words < 0,
+ *   bitmask_stride < bitmask_words, vocab_size > cols,
+ *   vocab_size > bitmask_words * 32, num_indices < 0, NULL logits/bitmask with
+ *   work to do, num_indices > 0 with NULL indices, bitmask_rows < B without
+ *   indices.
+ */
+lp_status lp_apply_token_bitmask(void* logits, lp_dtype dt, int64_t B, int64_t cols,
+                                 int64_t logits_stride, const int32_t* bitmask,
+                                 int64_t bitmask_rows, int64_t bitmask_words,
+                                 int64_t bitmask_stride, int64_t vocab_size,
+                                 const int32_t* indices, int64_t num_indices,
+                                 cudaStream_t stream);
+
+/*
+ * lp_apply_packed_bitmask -- Modular MAX "apply_packed_bitmask": one fused pass,
+ * no boolean tensor; out[b, v] = logits[b, v] where the bit is set, fill_value
+ * where it is clear.
+ *
+ * out receives all B rows x cols columns: the masked result on selected rows for
+ * j < vocab_size, a copy of logits everywhere else (unselected rows, columns >=
+ * vocab_size).  fill_value is rounded to nearest even into dt.  out may be
+ * exactly logits (same pointer and stride: in place); any other overlap is
+ * invalid and not detected.  Argument checks as lp_apply_token_bitmask, plus
+ * out_stride >= cols and a non-NULL out.
+ */
+lp_status lp_apply_packed_bitmask(void* out, int64_t out_stride, const void* logits,
+                                  lp_dtype dt, int64_t B, int64_t cols,
+                                  int64_t logits_stride, const int32_t* bitmask,
+                                  int64_t bitmask_rows, int64_t bitmask_words,
+                                  int64_t bitmask_stride, float fill_value,
+                                  int64_t vocab_size, const int32_t* indices,
+                                  int64_t num_indices, cudaStream_t stream);
+
+/*
+ * lp_sample -- Kernel Hub "logits-processor", Ops (sample) and How it works.
+ *
+ * One token id per row of logits[B, vocab_size] (row stride logits_stride):
+ *   candidates C = tokens with a finite-or-+inf logit above -inf;
+ *   C empty -> -1;
+ *   greedy (temperature <= 0 or top_k == 1) -> lowest-index argmax of the logits;
+ *   else z = logit / temperature, p = softmax(z) over C, keep every v in C with
+ *   p_v >= min(max(t_k, t_p, t_m), p_max), where t_k is the k-th largest p,
+ *   t_p the p at which the descending cumulative sum first reaches top_p and
+ *   t_m = min_p * p_max (a disabled filter contributes 0); the id is
+ *   argmax over kept v of z_v + g_v, lowest index on ties, with Gumbel noise
+ *   g_v = -log(-log u_v), u_v = ((x >> 9) + 0.5) * 2^-23 and x = word (v & 3) of
+ *   Philox4x32-10 (Salmon et al., SC'11) at counter (v >> 2, b, lo32(offset),
+ *   hi32(offset)) and key (lo32(seed), hi32(seed)).
+ *   out_ids        device int64 [B]
+ *   params         host pointer, see lp_sampling_params
+ * Logits are read only.  Rows longer than the sampler's on-chip capacity
+ * (LP_MAX_SAMPLE_ROW_BYTES of logits) return LP_ERR_TOO_LARGE.
+ */
+#define LP_MAX_SAMPLE_ROW_BYTES (8 * 200 * 1024)
+
+lp_status lp_sample(const void* logits, lp_dtype dt, int64_t B, int64_t vocab_size,
+                    int64_t logits_stride, const lp_sampling_params* params,
+                    int64_t* out_ids, cudaStream_t stream);
+
+/*
+ * lp_mask_and_sample -- the bitmask of lp_apply_token_bitmask applied on the fly
+ * (masked tokens leave the candidate set; logits are NOT written), then
+ * lp_sample.  A masked row whose mask admits no token returns -1
+ * (TensorRT-Edge-LLM "Guided Decoder": rowHasAnyToken / unsatisfiableSlots).
+ * Rows listed in indices are masked by their own bitmask row, other rows sample
+ * unmasked; indices == NULL masks every row.  bitmask == NULL is lp_sample.
+ * Argument checks as lp_apply_token_bitmask and lp_sample.
+ */
+lp_status lp_mask_and_sample(const void* logits, lp_dtype dt, int64_t B, int64_t cols,
+                             int64_t logits_stride, const int32_t* bitmask,
+                             int64_t bitmask_rows, int64_t bitmask_words,
+                             int64_t bitmask_stride, int64_t vocab_size,
+                             const int32_t* indices, int64_t num_indices,
+                             const lp_sampling_params* params, int64_t* out_ids,
+                             cudaStream_t stream);
+
+/*
+ * lp_philox4x32_10 -- diagnostic: the device's Philox4x32-10 (Salmon et al.,
+ * SC'11, 10 rounds) evaluated on n caller-given blocks, so tests can compare the
+ * noise stream of lp_sample word for word.
+ *   counters  device uint32 [n, 4];  keys  device uint32 [n, 2];
+ *   out       device uint32 [n, 4]
+ */
+lp_status lp_philox4x32_10(const uint32_t* counters, const uint32_t* keys, uint32_t* out,
+                           int64_t n, cudaStream_t stream);
+
+/* Static description of a status code; never NULL. */
+const char* lp_status_string(lp_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LP_H_ */

@@ -69,7 +69,7 @@ def load_library(path: str):
                               ctypes.c_float, i64, vp, i64]
     lib.lpo_mask_and_sample.restype = i32
     lib.lpo_mask_and_sample.argtypes = [vp, i32, i64, i64, i64, vp, i64, i64, i64, i64,
-                                        vp, i64, vp, vp, vp, vp, u64, u64, vp, vp, vp, vp]
+                                        vp, i64, vp, vp, vp, vp, u64, u64, vp, vp, vp, vp, vp]
     lib.lpo_philox4x32_10.restype = None
     lib.lpo_philox4x32_10.argtypes = [vp, vp, vp]
     lib.lpo_random_word.restype = u32
@@ -139,12 +139,15 @@ def _per_row(x, B, dt):
 
 def mask_and_sample(logits: np.ndarray, *, dtype: int, bitmask=None, vocab_size=None,
                     indices=None, cols=None, temperature=1.0, top_k=0, top_p=1.0, min_p=0.0,
-                    seed: int = 0, offset: int = 0, want_keep: bool = False,
+                    seed: int = 0, offset: int = 0, row_ids=None, want_keep: bool = False,
                     want_p: bool = False, want_thr: bool = False):
     """Per-row greedy / filtered Gumbel-max sampling (double precision).
 
-    Returns ids (int64 [B]) and, when asked, keep flags [B, V] (bool),
-    probabilities [B, V] and thresholds [B] as a tuple (ids, keep, p, thr)."""
+    ``row_ids`` (optional, one per array row) gives each row's logical index,
+    which keys the noise and addresses the bitmask (default 0..B-1), so a subset
+    of a batch can be checked on its own.  Returns ids (int64 [B]) and, when
+    asked, keep flags [B, V] (bool), probabilities [B, V] and thresholds [B] as a
+    tuple (ids, keep, p, thr)."""
     lib = _load()
     logits = np.ascontiguousarray(logits)
     B, stride = logits.shape
@@ -160,6 +163,8 @@ def mask_and_sample(logits: np.ndarray, *, dtype: int, bitmask=None, vocab_size=
     K = _per_row(top_k, B, np.int32)
     P = _per_row(top_p, B, np.float32)
     M = _per_row(min_p, B, np.float32)
+    rid = None if row_ids is None else np.ascontiguousarray(row_ids, dtype=np.int64)
+    assert rid is None or rid.shape == (B,)
     ids = np.empty(B, dtype=np.int64)
     keep = np.empty((B, V), dtype=np.uint8) if want_keep else None
     p = np.empty((B, V), dtype=np.float64) if want_p else None
@@ -168,8 +173,8 @@ def mask_and_sample(logits: np.ndarray, *, dtype: int, bitmask=None, vocab_size=
         _ptr(logits), dtype, B, cols, stride, _ptr(bm), 0 if bm is None else bm.shape[0],
         words, words, -1 if vocab_size is None else int(vocab_size), _ptr(idx),
         0 if idx is None else idx.size, _ptr(T), _ptr(K), _ptr(P), _ptr(M),
-        int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), _ptr(ids), _ptr(keep), _ptr(p),
-        _ptr(thr))
+        int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), _ptr(rid), _ptr(ids), _ptr(keep),
+        _ptr(p), _ptr(thr))
     if rc != 0:
         raise ValueError("inconsistent geometry")
     if not (want_keep or want_p or want_thr):

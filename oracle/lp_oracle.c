@@ -373,18 +373,20 @@ static int lpo_row(const double* l, const uint8_t* allowed, int64_t V, uint64_t 
 }
 
 /* Fused mask + sample over B rows (plain sample when bitmask == NULL).
-   Row b is masked by its own bitmask row when indices == NULL (every row) or when
-   b appears in indices[0..num_indices); other rows sample unmasked.  Per-row
-   parameters are full arrays of length B.  Optional outputs (NULL to skip):
-   keep_out [B, vocab_size], p_out [B, vocab_size], thr_out [B].
+   Row b of the arrays is logical row r = row_ids ? row_ids[b] : b: r keys the
+   noise, and the row is masked by bitmask row r when indices == NULL (every row)
+   or when r appears in indices[0..num_indices); other rows sample unmasked.  The
+   bitmask is addressed by the logical row.  Per-row parameters are full arrays of
+   length B.  Optional outputs (NULL to skip): keep_out [B, vocab_size],
+   p_out [B, vocab_size], thr_out [B].
    Returns 0, or -1 for an inconsistent geometry / allocation failure. */
 int lpo_mask_and_sample(const void* logits, int dtype, int64_t B, int64_t cols,
                         int64_t logits_stride, const int32_t* bitmask, int64_t bitmask_rows,
                         int64_t bitmask_words, int64_t bitmask_stride, int64_t vocab_size,
                         const int32_t* indices, int64_t num_indices, const float* temperature,
                         const int32_t* top_k, const float* top_p, const float* min_p,
-                        uint64_t seed, uint64_t offset, int64_t* ids_out, uint8_t* keep_out,
-                        double* p_out, double* thr_out) {
+                        uint64_t seed, uint64_t offset, const int64_t* row_ids,
+                        int64_t* ids_out, uint8_t* keep_out, double* p_out, double* thr_out) {
   if (bitmask)
     vocab_size = lpo_resolve_vocab(vocab_size, cols, bitmask_words);
   else if (vocab_size < 0)
@@ -400,21 +402,22 @@ int lpo_mask_and_sample(const void* logits, int dtype, int64_t B, int64_t cols,
   }
   int rc = 0;
   for (int64_t b = 0; b < B && rc == 0; ++b) {
+    const int64_t r = row_ids ? row_ids[b] : b;
     int masked = 0;
     if (bitmask) {
       if (!indices) {
         masked = 1;
       } else {
         for (int64_t i = 0; i < num_indices; ++i)
-          if ((int64_t)indices[i] == b) masked = 1;
+          if ((int64_t)indices[i] == r) masked = 1;
       }
-      if (b >= bitmask_rows) masked = 0;
+      if (r < 0 || r >= bitmask_rows) masked = 0;
     }
     for (int64_t j = 0; j < V; ++j) {
       l[j] = lpo_value(logits, dtype, b * logits_stride + j);
-      allowed[j] = masked ? (uint8_t)lpo_bit(bitmask, bitmask_stride, b, j) : 1;
+      allowed[j] = masked ? (uint8_t)lpo_bit(bitmask, bitmask_stride, r, j) : 1;
     }
-    rc = lpo_row(l, allowed, V, (uint64_t)b, (double)temperature[b], top_k[b],
+    rc = lpo_row(l, allowed, V, (uint64_t)r, (double)temperature[b], top_k[b],
                  (double)top_p[b], (double)min_p[b], seed, offset, &ids_out[b],
                  keep_out ? keep_out + b * V : NULL, p_out ? p_out + b * V : NULL,
                  thr_out ? thr_out + b : NULL);

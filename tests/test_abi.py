@@ -1,0 +1,154 @@
+"""The C-ABI library builds, loads, exports every entry point include/*.h
+declares, and rejects bad arguments on the host.
+
+No test here launches a kernel: every call either fails host-side validation or
+has no work, so none reaches the GPU (these run without one).
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+from grammar_constrained_logit_gb300 import _lib, build  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(lp_\w+)\s*\(", text, re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_header_declares_the_entry_points():
+    assert set(_lib.EXPORTS) <= _declared()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        s = lib.lp_status_string(code)
+        assert s and isinstance(s, bytes)
+    assert lib.lp_status_string(99) == b"unknown status"
+
+
+FAKE = ctypes.c_void_p(0x1000)  # never dereferenced: every call below fails validation
+
+
+def _apply(lib, **kw):
+    a = dict(logits=FAKE, dt=2, B=4, cols=64, stride=64, bm=FAKE, bm_rows=4, words=2,
+             bm_stride=2, vocab=-1, idx=None, n=0)
+    a.update(kw)
+    return lib.lp_apply_token_bitmask(a["logits"], a["dt"], a["B"], a["cols"], a["stride"],
+                                      a["bm"], a["bm_rows"], a["words"], a["bm_stride"],
+                                      a["vocab"], a["idx"], a["n"], None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(B=-1), dict(cols=-1), dict(stride=63), dict(words=-1), dict(bm_stride=1),
+    dict(vocab=65), dict(vocab=70, words=2, cols=100, stride=100), dict(n=-1),
+    dict(n=3, idx=None), dict(bm_rows=3), dict(bm_rows=-1), dict(logits=None),
+    dict(bm=None),
+])
+def test_apply_rejects(lib, kw):
+    assert _apply(lib, **kw) == _lib.LP_ERR_INVALID_ARGUMENT
+
+
+def test_apply_unsupported_dtype(lib):
+    assert _apply(lib, dt=7) == _lib.LP_ERR_UNSUPPORTED_DTYPE
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(vocab=0), dict(idx=FAKE, n=0),
+                                dict(B=0, logits=None, bm=None)])
+def test_apply_no_work_is_ok(lib, kw):
+    assert _apply(lib, **kw) == _lib.LP_OK
+
+
+def _oop(lib, **kw):
+    a = dict(out=ctypes.c_void_p(0x2000), out_stride=64, logits=FAKE, dt=0, B=4, cols=64,
+             stride=64, bm=FAKE, bm_rows=4, words=2, bm_stride=2, fill=-1.0, vocab=-1,
+             idx=None, n=0)
+    a.update(kw)
+    return lib.lp_apply_packed_bitmask(a["out"], a["out_stride"], a["logits"], a["dt"], a["B"],
+                                       a["cols"], a["stride"], a["bm"], a["bm_rows"],
+                                       a["words"], a["bm_stride"], a["fill"], a["vocab"],
+                                       a["idx"], a["n"], None)
+
+
+@pytest.mark.parametrize("kw", [dict(out_stride=10), dict(out=None), dict(logits=None),
+                                dict(bm=None), dict(stride=3), dict(vocab=100)])
+def test_out_of_place_rejects(lib, kw):
+    assert _oop(lib, **kw) == _lib.LP_ERR_INVALID_ARGUMENT
+
+
+def test_out_of_place_no_work(lib):
+    assert _oop(lib, B=0) == _lib.LP_OK
+    assert _oop(lib, cols=0, stride=0, out_stride=0) == _lib.LP_OK
+
+
+def _params():
+    p = _lib.SamplingParams()
+    p.temperature_scalar, p.top_k_scalar, p.top_p_scalar, p.min_p_scalar = 1.0, 0, 1.0, 0.0
+    return p
+
+
+def test_sample_validation(lib):
+    p = _params()
+    out = ctypes.c_void_p(0x3000)
+    assert lib.lp_sample(FAKE, 0, -1, 10, 10, ctypes.byref(p), out, None) == \
+        _lib.LP_ERR_INVALID_ARGUMENT
+    assert lib.lp_sample(FAKE, 0, 2, 10, 9, ctypes.byref(p), out, None) == \
+        _lib.LP_ERR_INVALID_ARGUMENT
+    assert lib.lp_sample(FAKE, 5, 2, 10, 10, ctypes.byref(p), out, None) == \
+        _lib.LP_ERR_UNSUPPORTED_DTYPE
+    assert lib.lp_sample(FAKE, 0, 2, 10, 10, None, out, None) == _lib.LP_ERR_INVALID_ARGUMENT
+    assert lib.lp_sample(FAKE, 0, 2, 10, 10, ctypes.byref(p), None, None) == \
+        _lib.LP_ERR_INVALID_ARGUMENT
+    assert lib.lp_sample(None, 0, 0, 10, 10, ctypes.byref(p), None, None) == _lib.LP_OK
+    # rows past the sampler's on-chip capacity are refused before any launch
+    huge = 8 * 200 * 1024 // 2 + 64
+    assert lib.lp_sample(FAKE, 1, 2, huge, huge, ctypes.byref(p), out, None) == \
+        _lib.LP_ERR_TOO_LARGE
+
+
+def test_mask_and_sample_validation(lib):
+    p = _params()
+    out = ctypes.c_void_p(0x3000)
+    call = lambda **kw: lib.lp_mask_and_sample(  # noqa: E731
+        kw.get("logits", FAKE), 2, kw.get("B", 4), kw.get("cols", 64), kw.get("stride", 64),
+        kw.get("bm", FAKE), kw.get("bm_rows", 4), kw.get("words", 2), kw.get("bm_stride", 2),
+        kw.get("vocab", -1), kw.get("idx", None), kw.get("n", 0), ctypes.byref(p), out, None)
+    assert call(vocab=65) == _lib.LP_ERR_INVALID_ARGUMENT
+    assert call(bm_rows=3) == _lib.LP_ERR_INVALID_ARGUMENT
+    assert call(n=2) == _lib.LP_ERR_INVALID_ARGUMENT
+    assert call(bm_stride=1) == _lib.LP_ERR_INVALID_ARGUMENT
+    assert call(stride=10) == _lib.LP_ERR_INVALID_ARGUMENT
+    assert call(B=0) == _lib.LP_OK
+
+
+def test_philox_validation(lib):
+    assert lib.lp_philox4x32_10(None, None, None, -1, None) == _lib.LP_ERR_INVALID_ARGUMENT
+    assert lib.lp_philox4x32_10(None, None, None, 0, None) == _lib.LP_OK
+    assert lib.lp_philox4x32_10(None, FAKE, FAKE, 3, None) == _lib.LP_ERR_INVALID_ARGUMENT
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        _lib.load(str(tmp_path / "nope.so"))

@@ -1,0 +1,393 @@
+"""Fused mask + sample on the GPU against the CPU oracle.
+
+The bar (greedy and masking exact; sampling by the stated tolerance):
+  * greedy ids (temperature <= 0, top_k == 1) identical to the oracle, lowest
+    index on ties; unsatisfiable rows -1;
+  * the device Philox4x32-10 identical to the oracle's, word for word;
+  * every sampled id accepted: in the oracle keep-set K, or with probability
+    within 1e-6 (relative) of the threshold, or in K' (the keep-set with top_p
+    raised and min_p lowered by 1e-6 relative);
+  * ids identical to the oracle's on >= 99.9% of rows (same noise stream);
+  * draw histograms within total variation 0.002 of the oracle's on the same
+    streams, and a goodness-of-fit to the exact filtered softmax;
+  * deterministic in (seed, offset), different when either changes;
+  * heterogeneous per-row parameters equal to broadcasting each row's own.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+from grammar_constrained_logit_gb300 import ops  # noqa: E402
+from grammar_constrained_logit_gb300 import synthetic as syn  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+DT = {"f32": oracle.F32, "f16": oracle.F16, "bf16": oracle.BF16}
+REL = 1e-6
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from grammar_constrained_logit_gb300 import _lib
+
+    _lib.load()
+
+
+def to_dev(storage: np.ndarray, dtype: str) -> torch.Tensor:
+    if dtype == "bf16":
+        return torch.from_numpy(storage.view(np.int16)).cuda().view(torch.bfloat16)
+    return torch.from_numpy(storage).cuda()
+
+
+def params_of(w: syn.Workload, rows=None):
+    out = {}
+    for name in ("temperature", "top_k", "top_p", "min_p"):
+        a = w.per_row(name)
+        out[name] = a if rows is None else a[rows]
+    return out
+
+
+def run_gpu(w: syn.Workload, offset: int, use_mask=True):
+    lg = to_dev(w.logits, w.dtype)[:, :w.cols]
+    p = {k: torch.from_numpy(v).cuda() for k, v in params_of(w).items()}
+    bm = torch.from_numpy(w.bitmask).cuda() if (use_mask and w.bitmask is not None) else None
+    idx = None if w.indices is None else torch.from_numpy(w.indices).cuda()
+    ids = ops.mask_and_sample(lg, bm, p["temperature"], p["top_k"], p["top_p"], p["min_p"],
+                              seed=w.seed, offset=offset, indices=idx,
+                              vocab_size=w.vocab_size if bm is not None else None)
+    return ids.cpu().numpy()
+
+
+def run_oracle(w: syn.Workload, offset: int, rows=None, relaxed=False, use_mask=True):
+    rows = np.arange(w.B) if rows is None else np.asarray(rows)
+    pr = params_of(w, rows)
+    tp, mp = pr["top_p"], pr["min_p"]
+    if relaxed:
+        tp = np.where(tp < 1, np.minimum(tp * (1 + REL), np.float32(0.99999994)), tp).astype(np.float32)
+        mp = (mp * (1 - REL)).astype(np.float32)
+    return oracle.mask_and_sample(
+        w.logits[rows], dtype=DT[w.dtype], bitmask=w.bitmask if use_mask else None,
+        vocab_size=w.vocab_size, indices=w.indices if use_mask else None, cols=w.cols,
+        temperature=pr["temperature"], top_k=pr["top_k"], top_p=tp, min_p=mp, seed=w.seed,
+        offset=offset, row_ids=rows, want_keep=True, want_p=True, want_thr=True)
+
+
+def check_rows(w, offset, gpu_ids, rows=None, min_agree=0.999, use_mask=True):
+    """Acceptance of every row plus the id-agreement rate."""
+    rows = np.arange(w.B) if rows is None else np.asarray(rows)
+    ids, keep, p, thr = run_oracle(w, offset, rows, use_mask=use_mask)
+    _, keep2, _, _ = run_oracle(w, offset, rows, relaxed=True, use_mask=use_mask)
+    g = gpu_ids[rows]
+    bad = []
+    for i, r in enumerate(rows):
+        v = int(g[i])
+        if ids[i] < 0 or thr[i] < 0:       # unsatisfiable or greedy: exact
+            if v != ids[i]:
+                bad.append((int(r), v, int(ids[i]), "exact"))
+            continue
+        ok = 0 <= v < keep.shape[1] and (keep[i, v] or keep2[i, v] or
+                                         p[i, v] >= thr[i] * (1 - REL))
+        if not ok:
+            bad.append((int(r), v, int(ids[i]), float(p[i, v]) if 0 <= v < p.shape[1] else None,
+                        float(thr[i])))
+    assert not bad, bad[:10]
+    agree = float(np.mean(g == ids))
+    assert agree >= min_agree, agree
+    return agree
+
+
+# ------------------------------------------------------------------- Philox
+
+def test_philox_words_identical():
+    rng = np.random.default_rng(3)
+    n = 20000
+    ctr = rng.integers(0, 2**32, size=(n, 4), dtype=np.uint64).astype(np.uint32)
+    key = rng.integers(0, 2**32, size=(n, 2), dtype=np.uint64).astype(np.uint32)
+    ctr[0] = 0
+    key[0] = 0
+    got = ops.philox4x32_10(torch.from_numpy(ctr.view(np.int32)).cuda(),
+                            torch.from_numpy(key.view(np.int32)).cuda()).cpu().numpy().view(np.uint32)
+    for i in range(0, n, 7):
+        assert got[i].tolist() == oracle.philox4x32_10(ctr[i], key[i]).tolist(), i
+
+
+# ------------------------------------------------------------------- golden
+
+def test_golden_keep_sets_and_greedy():
+    g = json.load(open(os.path.join(GOLDEN, "keep_set_small.json")))
+    for case in g["cases"]:
+        l = (np.log(np.array(case["probs"], dtype=np.float64)).astype(np.float32)
+             if "probs" in case else np.array([float(x) for x in case["logits"]], np.float32))
+        x = torch.from_numpy(np.tile(l, (64, 1))).cuda()
+        bm = None
+        if case.get("mask_bits") is not None:
+            bm = torch.from_numpy(np.tile(syn.pack_bits(np.array([case["mask_bits"]], bool)),
+                                          (64, 1))).cuda()
+        for off in range(4):
+            ids = ops.mask_and_sample(x, bm, case["T"], case["top_k"], case["top_p"],
+                                      case["min_p"], seed=11, offset=off).cpu().numpy()
+            assert set(ids.tolist()) <= set(case["kept"]), case["name"]
+    for case in g["greedy_cases"]:
+        l = np.array([float(x) for x in case["logits"]], np.float32)
+        x = torch.from_numpy(l[None, :]).cuda()
+        bm = None
+        if case.get("mask_bits") is not None:
+            bm = torch.from_numpy(syn.pack_bits(np.array([case["mask_bits"]], bool))).cuda()
+        ids = ops.mask_and_sample(x, bm, case["T"], case["top_k"]).cpu().numpy()
+        assert ids[0] == case["id"], case["name"]
+
+
+# ------------------------------------------------------------------- greedy
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("V", [1, 31, 1003, 32000, 131072, 202048])
+def test_greedy_exact(dtype, V):
+    rng = np.random.default_rng(V + DT[dtype])
+    B = 16
+    x = (rng.standard_normal((B, V)) * 2).astype(np.float32)
+    x[: B // 2] = np.round(x[: B // 2])          # exact ties everywhere
+    x[1, :] = 5.0                                # a row of all-equal values
+    x[2, :] = -np.inf                            # no finite candidate
+    allowed = rng.random((B, V)) < 0.3
+    allowed[3] = False                           # unsatisfiable
+    st = syn.to_storage(x, dtype)
+    bm = syn.pack_bits(allowed)
+    lg = to_dev(st, dtype)
+    bmd = torch.from_numpy(bm).cuda()
+    for temp, k in ((0.0, 0), (-1.0, 7), (0.8, 1)):
+        got = ops.mask_and_sample(lg, bmd, temp, k).cpu().numpy()
+        want = oracle.mask_and_sample(st, dtype=DT[dtype], bitmask=bm, temperature=temp, top_k=k)
+        assert np.array_equal(got, want), (temp, k, np.flatnonzero(got != want)[:5])
+        got = ops.sample(lg, temp, k).cpu().numpy()
+        want = oracle.mask_and_sample(st, dtype=DT[dtype], temperature=temp, top_k=k)
+        assert np.array_equal(got, want), (temp, k)
+
+
+def test_top_k_one_equals_greedy_equals_argmax():
+    rng = np.random.default_rng(4)
+    x = torch.from_numpy(rng.standard_normal((64, 50000)).astype(np.float32)).cuda()
+    a = ops.sample(x, 0.0).cpu().numpy()
+    b = ops.sample(x, 0.9, top_k=1, top_p=0.5, seed=3).cpu().numpy()
+    c = torch.argmax(x, dim=1).cpu().numpy()
+    assert np.array_equal(a, b) and np.array_equal(a, c)
+
+
+# ------------------------------------------------------- sampled parity
+
+def _small_workloads():
+    yield syn.tiny_greedy()
+    yield syn.apply_only(B=24, V=5000, padded_cols=5120, n_indexed=10, density=0.05)
+    yield syn.fused_sample(B=48, V=20000, steps=3)
+    for tp in (0.5, 0.9, 0.99):
+        yield syn.zipf_top_p(B=64, V=32000, top_p=tp)
+    yield syn.speculative_verify(slots=12, rows_per_slot=8, V=20000, constrained_slots=6)
+
+
+def test_small_workloads_parity():
+    total, agree = 0, 0.0
+    for w in _small_workloads():
+        if w.name == "apply_only":   # no sampling parameters: sample it plainly
+            w.temperature, w.top_k, w.top_p, w.min_p = 0.9, 40, 0.95, 0.01
+        for off in w.offsets[:3]:
+            g = run_gpu(w, off)
+            a = check_rows(w, off, g, min_agree=0.97)
+            agree += a * w.B
+            total += w.B
+    assert agree / total >= 0.999, agree / total
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_filter_grid_parity(dtype):
+    """Every combination of filters, on rows narrow and flat, masked and not,
+    including flat rows whose keep-set overflows the compaction buffers."""
+    rng = np.random.default_rng(77 + DT[dtype])
+    B, V = 96, 60000
+    x = rng.standard_normal((B, V)).astype(np.float32) * np.float32(2.0)
+    x[::3] *= np.float32(0.05)                   # flat rows
+    st = syn.to_storage(x, dtype)
+    allowed = rng.random((B, V)) < 0.5
+    allowed[::4] = True
+    w = syn.Workload("grid", dtype, st, V, V, bitmask=syn.pack_bits(allowed), seed=5)
+    grid = [(k, tp, mp) for k in (0, 2, 50, 1000, 5000) for tp in (1.0, 0.3, 0.9, 0.999)
+            for mp in (0.0, 0.05)]
+    w.temperature = rng.uniform(0.4, 1.6, B).astype(np.float32)
+    sel = [grid[i % len(grid)] for i in range(B)]
+    w.top_k = np.array([s[0] for s in sel], np.int32)
+    w.top_p = np.array([s[1] for s in sel], np.float32)
+    w.min_p = np.array([s[2] for s in sel], np.float32)
+    for off in (0, 1):
+        check_rows(w, off, run_gpu(w, off), min_agree=0.98)
+
+
+def test_masked_token_never_drawn_and_indices():
+    rng = np.random.default_rng(8)
+    B, V = 64, 4099
+    x = torch.from_numpy(rng.standard_normal((B, V)).astype(np.float32) * 3).cuda()
+    allowed = rng.random((B, V)) < 0.02
+    bm = torch.from_numpy(syn.pack_bits(allowed)).cuda()
+    idx = np.array([3, 5, 7, 63, -4, 200, 5], dtype=np.int32)  # invalid and duplicate entries
+    masked_rows = {3, 5, 7, 63}
+    hit_unmasked = 0
+    for off in range(20):
+        ids = ops.mask_and_sample(x, bm, 1.0, seed=1, offset=off,
+                                  indices=torch.from_numpy(idx)).cpu().numpy()
+        full = ops.mask_and_sample(x, bm, 1.0, 0, 0.95, 0.0, seed=2, offset=off).cpu().numpy()
+        for r in range(B):
+            if r in masked_rows:
+                assert allowed[r, ids[r]]
+            else:
+                hit_unmasked += int(not allowed[r, ids[r]])
+            assert allowed[r, full[r]]
+    assert hit_unmasked > 0  # rows outside indices really are unmasked
+
+
+def test_unsatisfiable_rows_return_minus_one():
+    x = torch.randn(6, 3000, device="cuda")
+    bm = torch.full((6, 94), -1, dtype=torch.int32, device="cuda")
+    bm[1] = 0
+    bm[4] = 0
+    for args in ((0.0, 0), (1.0, 0), (0.7, 5, 0.9, 0.1), (1.3, 0, 1.0, 0.0)):
+        ids = ops.mask_and_sample(x, bm, *args).cpu().numpy()
+        assert ids[1] == -1 and ids[4] == -1 and (ids[[0, 2, 3, 5]] >= 0).all()
+
+
+def test_edge_shapes():
+    for B, V in ((1, 1), (3, 2), (2, 33), (5, 7)):
+        x = np.random.default_rng(V).standard_normal((B, V)).astype(np.float32)
+        for args in (dict(temperature=0.0), dict(temperature=1.0),
+                     dict(temperature=1.0, top_k=2, top_p=0.5, min_p=0.1)):
+            g = ops.sample(torch.from_numpy(x).cuda(), **args, seed=1).cpu().numpy()
+            w = oracle.mask_and_sample(x, dtype=oracle.F32, seed=1, **args)
+            assert np.array_equal(g, w), (B, V, args)
+    # zero-width vocabulary: every row has no candidate
+    ids = ops.sample(torch.randn(4, 8, device="cuda"), 1.0, vocab_size=0).cpu().numpy()
+    assert (ids == -1).all()
+    # empty batch: nothing launched
+    assert ops.sample(torch.randn(0, 8, device="cuda"), 1.0).numel() == 0
+
+
+def test_misaligned_rows_and_strides():
+    rng = np.random.default_rng(12)
+    for dtype in ("f32", "f16", "bf16"):
+        B, V, stride = 9, 3001, 3011
+        x = (rng.standard_normal((B, stride)) * 2).astype(np.float32)
+        st = syn.to_storage(x, dtype)
+        base = to_dev(np.concatenate([st.reshape(-1), st.reshape(-1)[:1]]), dtype)
+        lg = base[1:1 + B * stride].view(B, stride)[:, :V]     # base pointer off by one element
+        allowed = rng.random((B, V)) < 0.4
+        bm = syn.pack_bits(allowed)
+        for args in (dict(temperature=0.0), dict(temperature=0.9, top_k=30, top_p=0.9)):
+            got = ops.mask_and_sample(lg, torch.from_numpy(bm).cuda(), seed=4, **args).cpu().numpy()
+            shifted = np.concatenate([st.reshape(-1), st.reshape(-1)[:1]])[1:1 + B * stride]
+            want = oracle.mask_and_sample(shifted.reshape(B, stride), dtype=DT[dtype], bitmask=bm,
+                                          cols=V, seed=4, **args)
+            assert np.array_equal(got, want), (dtype, args)
+
+
+def test_longest_supported_row_and_limit():
+    from grammar_constrained_logit_gb300._lib import LPError
+
+    V = 800_000
+    rng = np.random.default_rng(13)
+    x = (rng.standard_normal((2, V)) * 2).astype(np.float32)
+    st = syn.to_storage(x, "bf16")
+    lg = to_dev(st, "bf16")
+    for args in (dict(temperature=0.0), dict(temperature=1.0, top_k=100),
+                 dict(temperature=1.0, top_p=0.5)):
+        got = ops.sample(lg, seed=9, **args).cpu().numpy()
+        want = oracle.mask_and_sample(st, dtype=oracle.BF16, seed=9, **args)
+        assert np.array_equal(got, want), args
+    with pytest.raises(LPError):
+        ops.sample(torch.zeros(1, 900_000, device="cuda", dtype=torch.bfloat16), 1.0)
+
+
+# ---------------------------------------------------- distribution, determinism
+
+def test_distribution_same_streams_and_exact():
+    from scipy import stats
+
+    V = 64
+    rng = np.random.default_rng(21)
+    l = (rng.standard_normal(V) * 1.5).astype(np.float32)
+    N = 100_000
+    x = np.tile(l, (N, 1))
+    for args in (dict(temperature=1.0), dict(temperature=0.7, top_k=10),
+                 dict(temperature=1.2, top_p=0.8), dict(temperature=1.0, min_p=0.1)):
+        g = ops.sample(torch.from_numpy(x).cuda(), seed=99, offset=5, **args).cpu().numpy()
+        o, keep, p, _ = oracle.mask_and_sample(x[:1], dtype=oracle.F32, seed=99, offset=5,
+                                               want_keep=True, want_p=True, **args)
+        o = oracle.mask_and_sample(x, dtype=oracle.F32, seed=99, offset=5, **args)
+        hg = np.bincount(g, minlength=V) / N
+        ho = np.bincount(o, minlength=V) / N
+        assert 0.5 * np.abs(hg - ho).sum() <= 0.002, args
+        q = np.where(keep[0], p[0], 0.0)
+        q /= q.sum()
+        assert hg[~keep[0]].sum() == 0
+        sel = keep[0]
+        cnt = hg[sel] * N
+        chi2 = ((cnt - N * q[sel]) ** 2 / (N * q[sel])).sum()
+        pval = stats.chi2.sf(chi2, df=max(int(sel.sum()) - 1, 1)) if sel.sum() > 1 else 1.0
+        assert pval > 1e-4, (args, chi2, pval)
+
+
+def test_determinism_and_offset():
+    w = syn.fused_sample(B=64, V=40000, steps=1)
+    a = run_gpu(w, 0)
+    b = run_gpu(w, 0)
+    c = run_gpu(w, 1)
+    w2 = syn.fused_sample(B=64, V=40000, steps=1)
+    w2.seed = 8
+    d = run_gpu(w2, 0)
+    assert np.array_equal(a, b)
+    assert (a != c).mean() > 0.3 and (a != d).mean() > 0.3
+
+
+def test_heterogeneous_rows_equal_broadcast():
+    w = syn.speculative_verify(slots=8, rows_per_slot=8, V=30000, constrained_slots=4)
+    het = run_gpu(w, 3)
+    pr = params_of(w)
+    lg = to_dev(w.logits, w.dtype)
+    bm = torch.from_numpy(w.bitmask).cuda()
+    idx = torch.from_numpy(w.indices).cuda()
+    for r in range(0, w.B, 5):
+        one = ops.mask_and_sample(lg, bm, float(pr["temperature"][r]), int(pr["top_k"][r]),
+                                  float(pr["top_p"][r]), float(pr["min_p"][r]), seed=w.seed,
+                                  offset=3, indices=idx).cpu().numpy()
+        assert one[r] == het[r], r
+
+
+# ------------------------------------------------------ full-size workloads
+
+def test_fused_sample_full_size():
+    """B=256, V=131072 bf16, 10% mask, per-row T, top_k 50, top_p 0.9, min_p 0.05."""
+    w = syn.fused_sample()
+    for off in (0, 57, 99):
+        check_rows(w, off, run_gpu(w, off))
+
+
+@pytest.mark.parametrize("tp", [0.5, 0.9, 0.99, "greedy"])
+def test_zipf_top_p_full_size(tp):
+    """B=1024, V=32000 fp32 Zipf-ranked logits, T=0.7, top_p sweep and greedy."""
+    w = syn.zipf_top_p(top_p=0.9 if tp == "greedy" else tp)
+    if tp == "greedy":
+        w.temperature = 0.0
+    check_rows(w, 0, run_gpu(w, 0))
+
+
+def test_speculative_verify_full_size_sampled_rows():
+    """1024 rows x 202048 fp16, 512 masked rows, heterogeneous parameters; every
+    row is drawn on the GPU, a seeded sample of 160 rows is checked."""
+    w = syn.speculative_verify()
+    g = run_gpu(w, 0)
+    rows = np.sort(np.random.default_rng(0).choice(w.B, size=160, replace=False))
+    rows = np.union1d(rows, w.indices[:8])
+    check_rows(w, 0, g, rows=rows, min_agree=0.99)
+    assert (g >= -1).all() and (g < w.vocab_size).all()
