@@ -52,14 +52,29 @@ def _bitmask(bitmask: torch.Tensor, device) -> torch.Tensor:
     return bm
 
 
+class _Indices:
+    """Row list marshalled for the C ABI.  An empty list still needs a non-NULL
+    pointer (NULL means "every row"), so it points at a one-element buffer."""
+
+    def __init__(self, t: torch.Tensor):
+        self.n = t.numel()
+        self.t = t if self.n else torch.empty(1, dtype=torch.int32, device=t.device)
+
+    def data_ptr(self):
+        return self.t.data_ptr()
+
+    def numel(self):
+        return self.n
+
+
 def _indices(indices, device):
     if indices is None:
         return None
     if isinstance(indices, torch.Tensor):
-        idx = indices.to(device=device, dtype=torch.int32).contiguous()
+        idx = indices.to(device=device, dtype=torch.int32).contiguous().view(-1)
     else:
         idx = torch.tensor(list(indices), dtype=torch.int32, device=device)
-    return idx
+    return _Indices(idx)
 
 
 def _ptr(t):
