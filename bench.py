@@ -1,0 +1,651 @@
+#!/usr/bin/env python
+"""Benchmark of the grammar-constrained logit path on GB300.
+
+Headline metric: bitmask-apply HBM throughput (GB/s, and its fraction of the
+measured HBM copy bandwidth) on the apply workload -- B=64 bf16 rows padded to
+128512 columns, vocab 128256, a 1%-dense grammar-like mask, 32 indexed rows --
+and the fused mask + sample rate (rows/s) on the sampling workload -- B=256,
+V=131072 bf16, 10% mask, per-row temperature, top_k 50, top_p 0.9, min_p 0.05.
+
+One step = one in-place apply over a batch of the first workload plus one fused
+mask + sample over a batch of the second.  Inputs are resident in HBM and rotate
+through rings of copies larger than four L2 caches, so no step reads a batch
+from L2.  Steps are captured in CUDA graphs (launch gaps are those of a graph
+replay) and timed with CUDA events on the launching stream; CUDA events between
+the apply and sample graph replays split the time per kernel.
+
+    python bench.py [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload default|apply_only|fused_sample|zipf_top_p|
+                                speculative_verify|tiny_greedy]
+
+Prints one JSON line.  ``--impl reference`` times the CPU oracle (single
+thread) on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from grammar_constrained_logit_gb300 import synthetic as syn  # noqa: E402
+
+METRIC = "apply_token_bitmask HBM GB/s (% of GB300 peak); fused mask+sample rows/s"
+EB = {"f32": 4, "f16": 2, "bf16": 2}
+
+
+# ------------------------------------------------------------ bytes per unit
+
+def apply_rows(w: syn.Workload) -> int:
+    if w.indices is None:
+        return w.B
+    return int(np.unique(w.indices[(w.indices >= 0) & (w.indices < min(w.B, w.bitmask.shape[0]))]).size)
+
+
+def apply_bytes(w: syn.Workload) -> int:
+    """In place: read + write of every applied logit, plus the mask words."""
+    rows = apply_rows(w)
+    return 2 * rows * w.vocab_size * EB[w.dtype] + rows * w.bitmask.shape[1] * 4
+
+
+def sample_bytes(w: syn.Workload, masked: bool = True) -> int:
+    """Fused mask + sample: each logit read once, the mask words of masked rows,
+    8 bytes of id per row."""
+    b = w.B * w.vocab_size * EB[w.dtype] + 8 * w.B
+    if masked and w.bitmask is not None:
+        b += apply_rows(w) * w.bitmask.shape[1] * 4
+    return b
+
+
+def describe(w: syn.Workload) -> str:
+    s = f"{w.name}: B={w.B}, V={w.vocab_size} {w.dtype}"
+    if w.cols != w.vocab_size or w.stride != w.cols:
+        s += f" (row stride {w.stride})"
+    if w.bitmask is not None:
+        s += f", mask [{w.bitmask.shape[0]}x{w.bitmask.shape[1]}]"
+    if w.indices is not None:
+        s += f", {apply_rows(w)} indexed rows"
+    return s
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_id: str | None):
+        self.proc = None
+        self.path = None
+        self.device_id = device_id
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "20"]
+        if self.device_id:
+            cmd += ["-i", self.device_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[3:]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        seen = set()
+        for _, _, flags in rows:
+            for n, f in zip(names, flags[1:5]):
+                if f.lower().startswith("active"):
+                    seen.add(n)
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": rows[0][1],
+                "reasons": sorted(seen), "samples": len(rows)}
+
+
+# --------------------------------------------------------------- helpers
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "grammar_constrained_logit_gb300", "csrc", "*"))):
+        h.update(open(f, "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "lp.h"), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken on the
+    current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    e = d.get("kernels", {}).get(f"{kernel}:{workload}")
+    return None if e is None else e.get("dram_bytes_per_launch")
+
+
+def make_workload(name: str) -> syn.Workload:
+    return syn.WORKLOADS[name]()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(value: float, device=None) -> float:
+    """Max of a float over all ranks (a timing reduction, not a data-path collective)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- GPU arm
+
+class Op:
+    """One hot-path call on one workload, with a ring of device input copies."""
+
+    def __init__(self, kind: str, w: syn.Workload, ring_bytes_min: int, torch, ops):
+        self.kind, self.w, self.torch, self.ops = kind, w, torch, ops
+        dev = torch.device("cuda")
+        st = w.logits
+        if w.dtype == "bf16":
+            host = torch.from_numpy(st.view(np.int16)).view(torch.bfloat16)
+        else:
+            host = torch.from_numpy(st)
+        touched = apply_bytes(w) if kind == "apply" else sample_bytes(w)
+        per_copy = st.nbytes + (0 if w.bitmask is None else w.bitmask.nbytes)
+        free = torch.cuda.mem_get_info()[0]
+        self.R = int(max(2, min(64, -(-ring_bytes_min // max(touched, 1)))))
+        self.R = max(2, min(self.R, int(0.25 * free // max(per_copy, 1))))
+        first = host.to(dev)
+        self.logits = [first] + [first.clone() for _ in range(self.R - 1)]
+        self.bitmask = None
+        if w.bitmask is not None:
+            b0 = torch.from_numpy(w.bitmask).to(dev)
+            self.bitmask = [b0] + [b0.clone() for _ in range(self.R - 1)]
+        self.indices = None if w.indices is None else torch.from_numpy(w.indices).to(dev)
+        self.params = {k: torch.from_numpy(w.per_row(k)).to(dev)
+                       for k in ("temperature", "top_k", "top_p", "min_p")}
+        self.out = torch.empty(w.B, dtype=torch.int64, device=dev)
+        self.bytes = touched
+        self.units = w.B
+
+    def launch(self, slot: int, step: int):
+        w, ops = self.w, self.ops
+        lg = self.logits[slot % self.R][:, :w.cols]
+        bm = None if self.bitmask is None else self.bitmask[slot % self.R]
+        if self.kind == "apply":
+            ops.apply_token_bitmask_inplace(lg, bm, vocab_size=w.vocab_size, indices=self.indices)
+        else:
+            p = self.params
+            ops.mask_and_sample(lg, bm, p["temperature"], p["top_k"], p["top_p"], p["min_p"],
+                                seed=w.seed, offset=w.offsets[step % len(w.offsets)],
+                                indices=self.indices,
+                                vocab_size=w.vocab_size if bm is not None else None,
+                                out=self.out)
+
+    def capture(self, nsteps: int, first_step: int):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.launch(0, 0)  # sets kernel attributes before capture
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            for j in range(nsteps):
+                self.launch(first_step + j, first_step + j)
+        return g
+
+
+def e2e_apply(w: syn.Workload, steps: int, torch, ops) -> dict:
+    """apply_token_bitmask_inplace through the public API, inputs from pinned
+    host memory and the result copied back, per step."""
+    dev = torch.device("cuda")
+    if w.dtype == "bf16":
+        host = torch.from_numpy(w.logits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    else:
+        host = torch.from_numpy(w.logits).pin_memory()
+    bm_h = torch.from_numpy(w.bitmask).pin_memory()
+    idx_h = None if w.indices is None else torch.from_numpy(w.indices).pin_memory()
+    out_h = torch.empty_like(host).pin_memory()
+    lg = torch.empty_like(host, device=dev)
+    bm = torch.empty_like(bm_h, device=dev)
+    idx = None if idx_h is None else torch.empty_like(idx_h, device=dev)
+
+    def step():
+        lg.copy_(host, non_blocking=True)
+        bm.copy_(bm_h, non_blocking=True)
+        if idx is not None:
+            idx.copy_(idx_h, non_blocking=True)
+        ops.apply_token_bitmask_inplace(lg[:, :w.cols], bm, vocab_size=w.vocab_size, indices=idx)
+        out_h.copy_(lg, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    sec = e0.elapsed_time(e1) / 1e3 / steps
+    h2d = host.numel() * host.element_size() + bm_h.numel() * 4 + (0 if idx_h is None else idx_h.numel() * 4)
+    return {"value": round(apply_bytes(w) / sec / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(out_h.numel() * out_h.element_size()),
+            "ms_per_step": round(sec * 1e3, 4)}
+
+
+def e2e_sample(w: syn.Workload, steps: int, torch, ops) -> dict:
+    dev = torch.device("cuda")
+    if w.dtype == "bf16":
+        host = torch.from_numpy(w.logits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    else:
+        host = torch.from_numpy(w.logits).pin_memory()
+    bm_h = None if w.bitmask is None else torch.from_numpy(w.bitmask).pin_memory()
+    idx_h = None if w.indices is None else torch.from_numpy(w.indices).pin_memory()
+    par_h = {k: torch.from_numpy(w.per_row(k)).pin_memory()
+             for k in ("temperature", "top_k", "top_p", "min_p")}
+    lg = torch.empty_like(host, device=dev)
+    bm = None if bm_h is None else torch.empty_like(bm_h, device=dev)
+    idx = None if idx_h is None else torch.empty_like(idx_h, device=dev)
+    par = {k: torch.empty_like(v, device=dev) for k, v in par_h.items()}
+    ids = torch.empty(w.B, dtype=torch.int64, device=dev)
+    ids_h = torch.empty(w.B, dtype=torch.int64).pin_memory()
+
+    def step(i):
+        lg.copy_(host, non_blocking=True)
+        if bm is not None:
+            bm.copy_(bm_h, non_blocking=True)
+        if idx is not None:
+            idx.copy_(idx_h, non_blocking=True)
+        for k in par:
+            par[k].copy_(par_h[k], non_blocking=True)
+        ops.mask_and_sample(lg[:, :w.cols], bm, par["temperature"], par["top_k"], par["top_p"],
+                            par["min_p"], seed=w.seed, offset=w.offsets[i % len(w.offsets)],
+                            indices=idx, vocab_size=w.vocab_size if bm is not None else None,
+                            out=ids)
+        ids_h.copy_(ids, non_blocking=True)
+
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        step(i)
+    e1.record()
+    torch.cuda.synchronize()
+    sec = e0.elapsed_time(e1) / 1e3 / steps
+    h2d = host.numel() * host.element_size() + (0 if bm_h is None else bm_h.numel() * 4) + \
+        (0 if idx_h is None else idx_h.numel() * 4) + sum(v.numel() * 4 for v in par_h.values())
+    return {"value": round(w.B / sec, 1), "unit": "rows/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(8 * w.B), "ms_per_step": round(sec * 1e3, 4)}
+
+
+def roofline(bytes_per_launch: int, sec_per_launch: float, peak: dict, traffic) -> dict:
+    achieved = bytes_per_launch / sec_per_launch / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak["hbm_gbs"],
+            "unit": "GB/s", "frac": round(achieved / peak["hbm_gbs"], 4),
+            "peak_source": peak["source"], "traffic": traffic,
+            "algorithmic_bytes_per_launch": int(bytes_per_launch),
+            "us_per_launch": round(sec_per_launch * 1e6, 3)}
+
+
+def run_gpu(args) -> dict | None:
+    import torch
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from grammar_constrained_logit_gb300 import ops
+    from grammar_constrained_logit_gb300 import _lib
+
+    _lib.load()
+    dev_props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    l2 = int(getattr(dev_props, "L2_cache_size", 128 << 20))
+    ring_min = 4 * l2
+
+    plan = []  # (op, units label)
+    if args.workload == "default":
+        wa, wf = make_workload("apply_only"), make_workload("fused_sample")
+        plan = [Op("apply", wa, ring_min, torch, ops), Op("sample", wf, ring_min, torch, ops)]
+    elif args.workload == "apply_only":
+        plan = [Op("apply", make_workload("apply_only"), ring_min, torch, ops)]
+    elif args.workload == "tiny_greedy":
+        w = make_workload("tiny_greedy")
+        plan = [Op("apply", w, ring_min, torch, ops), Op("sample", w, ring_min, torch, ops)]
+    else:
+        w = make_workload(args.workload)
+        if args.workload == "zipf_top_p":
+            if args.top_p == "greedy":
+                w.temperature = 0.0
+            else:
+                w.top_p = float(args.top_p)
+        plan = [Op("sample", w, ring_min, torch, ops)]
+
+    K, W = args.steps, args.warmup
+    G = max(1, min(args.graph_steps, K))
+    graphs = [op.capture(G, 0) for op in plan]
+    rem = K % G
+    rem_graphs = [op.capture(rem, (K // G) * G) for op in plan] if rem else None
+
+    for _ in range(max(1, -(-W // G))):
+        for g in graphs:
+            g.replay()
+    torch.cuda.synchronize()
+
+    dev_id = None
+    try:
+        dev_id = str(dev_props.uuid)
+        if not dev_id.startswith("GPU-"):
+            dev_id = "GPU-" + dev_id
+    except Exception:  # noqa: BLE001
+        dev_id = os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0] or None
+    sampler = ClockSampler(dev_id)
+    sampler.start()
+    barrier()
+    torch.cuda.synchronize()
+    reps = K // G
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in plan] for _ in range(reps + (1 if rem else 0))]
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_start.record()
+    for r in range(reps):
+        for i, g in enumerate(graphs):
+            marks[r][i].record()
+            g.replay()
+    if rem:
+        for i, g in enumerate(rem_graphs):
+            marks[reps][i].record()
+            g.replay()
+    e_end.record()
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+
+    total_s = e_start.elapsed_time(e_end) / 1e3
+    per_op = [0.0] * len(plan)
+    flat = [m for row in marks for m in row] + [e_end]
+    for j in range(len(flat) - 1):
+        per_op[j % len(plan)] += flat[j].elapsed_time(flat[j + 1]) / 1e3
+    total_s = reduce_max(total_s, torch.device("cuda"))
+    per_op = [reduce_max(t, torch.device("cuda")) for t in per_op]
+    if rank != 0:
+        return None
+
+    peak = measured_peaks()
+    res = {"metric": METRIC, "n_gpus": ws, "steps": K, "warmup": W,
+           "ms_per_step": round(total_s / K * 1e3, 5), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": plan[0].w.dtype,
+           "data": "synthetic (seeded generators shaped like the pages' workloads)",
+           "gpu_launches": K * len(plan) * ws}
+    cfg = {"workload": " + ".join(describe(op.w) for op in plan),
+           "l2": f"inputs rotate through device rings (>= 4x the {l2 >> 20} MB L2) so no step "
+                 "reads its batch from L2",
+           "timing": f"CUDA graphs of {G} steps replayed; CUDA events on the launch stream",
+           "parallelism": f"replicas x{ws} (rows shard with no collective)"}
+    for op in plan:
+        cfg[f"ring_{op.kind}"] = op.R
+    res["config"] = cfg
+    lines = {}
+    for op, t in zip(plan, per_op):
+        sec = t / K
+        wl = op.w.name
+        kname = "apply_kernel" if op.kind == "apply" else "sample_kernel"
+        rf = roofline(op.bytes, sec, peak, ncu_traffic(kname, wl))
+        if op.kind == "apply":
+            lines["apply"] = {"value": round(op.bytes * ws / sec / 1e9, 2), "unit": "GB/s",
+                              "workload": describe(op.w), "roofline": rf}
+        else:
+            lines["sample"] = {"value": round(op.units * ws / sec, 1), "unit": "rows/s",
+                               "workload": describe(op.w), "roofline": rf,
+                               "GBps_algorithmic": rf["achieved"]}
+    if "apply" in lines:
+        res["value"] = lines["apply"]["value"]
+        res["unit"] = "GB/s"
+    else:
+        res["value"] = lines["sample"]["value"]
+        res["unit"] = "rows/s"
+    dominant = max(zip(plan, per_op), key=lambda x: x[1])[0]
+    res["roofline"] = lines["apply" if dominant.kind == "apply" else "sample"]["roofline"]
+    res["roofline"]["kernel"] = "apply_kernel" if dominant.kind == "apply" else "sample_kernel"
+    if "apply" in lines:
+        res["apply"] = lines["apply"]
+    if "sample" in lines:
+        res["fused_mask_sample"] = lines["sample"]
+    res["clocks"] = clocks
+
+    if not args.no_e2e:
+        e2e = {}
+        for op in plan:
+            if op.kind == "apply":
+                e2e["apply"] = e2e_apply(op.w, args.e2e_steps, torch, ops)
+            else:
+                e2e["sample"] = e2e_sample(op.w, args.e2e_steps, torch, ops)
+        head = e2e.get("apply") or e2e.get("sample")
+        res["e2e"] = {"value": head["value"], "unit": head["unit"],
+                      "h2d_bytes_per_step": sum(v["h2d_bytes_per_step"] for v in e2e.values()),
+                      "d2h_bytes_per_step": sum(v["d2h_bytes_per_step"] for v in e2e.values()),
+                      "parts": e2e}
+    if not args.no_cpu_baseline and ws == 1:
+        res["cpu_baseline"] = cpu_baseline([op.w for op in plan], [op.kind for op in plan],
+                                           args.cpu_seconds)
+    return res
+
+
+# -------------------------------------------------------------- CPU oracle
+
+def _oracle_apply_rows(w: syn.Workload, nrows: int):
+    """Oracle apply restricted to the first nrows of the workload's row list."""
+    import oracle
+
+    idx = w.indices if w.indices is not None else np.arange(w.B, dtype=np.int32)
+    sub = idx[:nrows]
+    return lambda: oracle.apply(w.logits, w.bitmask, dtype={"f32": 0, "f16": 1, "bf16": 2}[w.dtype],
+                                vocab_size=w.vocab_size, indices=sub, cols=w.cols)
+
+
+def _oracle_sample_rows(w: syn.Workload, rows: np.ndarray, offset: int = 0):
+    import oracle
+
+    pr = {k: w.per_row(k)[rows] for k in ("temperature", "top_k", "top_p", "min_p")}
+    dt = {"f32": 0, "f16": 1, "bf16": 2}[w.dtype]
+    lg = np.ascontiguousarray(w.logits[rows])
+    return lambda: oracle.mask_and_sample(
+        lg, dtype=dt, bitmask=w.bitmask, vocab_size=w.vocab_size if w.bitmask is not None else None,
+        indices=w.indices, cols=w.cols, temperature=pr["temperature"], top_k=pr["top_k"],
+        top_p=pr["top_p"], min_p=pr["min_p"], seed=w.seed, offset=offset, row_ids=rows)
+
+
+def _time_for(fn, seconds: float):
+    fn()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= seconds:
+            return dt / n, n
+
+
+def cpu_baseline(workloads, kinds, seconds: float) -> dict:
+    """The oracle, as it stands (single thread), on bounded samples."""
+    out = {"kind": "oracle", "cores": 1}
+    per = seconds / max(len(workloads), 1)
+    for w, kind in zip(workloads, kinds):
+        if kind == "apply":
+            rows = apply_rows(w)
+            per_call, n = _time_for(_oracle_apply_rows(w, rows), per)
+            gbs = apply_bytes(w) / per_call / 1e9
+            out["apply"] = {"value": round(gbs, 4), "unit": "GB/s",
+                            "sample": f"{describe(w)}: all {rows} applied rows, {n} repeats"}
+        else:
+            nr = min(w.B, 16)
+            rows = np.sort(np.random.default_rng(0).choice(w.B, size=nr, replace=False))
+            per_call, n = _time_for(_oracle_sample_rows(w, rows), per)
+            out["sample"] = {"value": round(nr / per_call, 3), "unit": "rows/s",
+                             "sample": f"{describe(w)}: {nr} seeded rows, {n} repeats"}
+    head = out.get("apply") or out.get("sample")
+    out["value"], out["unit"], out["sample"] = head["value"], head["unit"], head["sample"]
+    return out
+
+
+def run_reference(args) -> dict | None:
+    """The oracle timed as the reference arm: each step one bounded sample of the
+    workload (apply rows and sampled rows sized so the run stays in minutes)."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+
+    oracle.build()
+    if args.workload in ("default",):
+        ws_list = [("apply", make_workload("apply_only")), ("sample", make_workload("fused_sample"))]
+    elif args.workload == "apply_only":
+        ws_list = [("apply", make_workload("apply_only"))]
+    elif args.workload == "tiny_greedy":
+        w = make_workload("tiny_greedy")
+        ws_list = [("apply", w), ("sample", w)]
+    else:
+        ws_list = [("sample", make_workload(args.workload))]
+    K, W = args.steps, args.warmup
+    budget = args.reference_seconds / max(K + W, 1)   # seconds per step
+    calls = []
+    for kind, w in ws_list:
+        if kind == "apply":
+            total_rows = apply_rows(w)
+            t1, _ = _time_for(_oracle_apply_rows(w, 1), 0.2)
+            nr = int(max(1, min(total_rows, budget / len(ws_list) / max(t1, 1e-9))))
+            fn = _oracle_apply_rows(w, nr)
+            frac = nr / total_rows
+            calls.append((kind, w, fn, apply_bytes(w) * frac, nr))
+        else:
+            t1, _ = _time_for(_oracle_sample_rows(w, np.array([0])), 0.2)
+            nr = int(max(1, min(w.B, budget / len(ws_list) / max(t1, 1e-9))))
+            rows = np.sort(np.random.default_rng(0).choice(w.B, size=nr, replace=False))
+            calls.append((kind, w, _oracle_sample_rows(w, rows), nr, nr))
+    times = [0.0] * len(calls)
+    for _ in range(W):
+        for _, _, fn, _, _ in calls:
+            fn()
+    for _ in range(K):
+        for i, (_, _, fn, _, _) in enumerate(calls):
+            t0 = time.perf_counter()
+            fn()
+            times[i] += time.perf_counter() - t0
+    res = {"impl": "reference", "metric": METRIC, "n_gpus": 1, "steps": K, "warmup": W,
+           "ms_per_step": round(sum(times) / max(K, 1) * 1e3, 4), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": ws_list[0][1].dtype,
+           "data": "synthetic (seeded generators shaped like the pages' workloads)",
+           "gpu_launches": 0}
+    parts = {}
+    for (kind, w, _, units, nr), t in zip(calls, times):
+        sec = t / max(K, 1)
+        if kind == "apply":
+            parts["apply"] = {"value": round(units / sec / 1e9, 4), "unit": "GB/s",
+                              "sample": f"{describe(w)}: {nr} of {apply_rows(w)} applied rows per step"}
+        else:
+            parts["sample"] = {"value": round(units / sec, 3), "unit": "rows/s",
+                               "sample": f"{describe(w)}: {nr} seeded rows per step"}
+    head = parts.get("apply") or parts.get("sample")
+    res["value"], res["unit"] = head["value"], head["unit"]
+    res["config"] = {"workload": " + ".join(describe(w) for _, w in ws_list),
+                     "parallelism": "single CPU thread"}
+    res["cpu_baseline"] = {"value": head["value"], "unit": head["unit"], "cores": 1,
+                           "kind": "oracle", "sample": head["sample"], "parts": parts}
+    res["e2e"] = {"value": head["value"], "unit": head["unit"], "h2d_bytes_per_step": 0,
+                  "d2h_bytes_per_step": 0}
+    if "sample" in parts and "apply" in parts:
+        res["fused_mask_sample"] = parts["sample"]
+    return res
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="default",
+                    choices=["default", *syn.WORKLOADS.keys()])
+    ap.add_argument("--top-p", default="0.9", help="zipf_top_p: 0.5, 0.9, 0.99 or greedy")
+    ap.add_argument("--graph-steps", type=int, default=100)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--reference-seconds", type=float, default=90.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    res = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -2,40 +2,48 @@
 // sampler (Kernel Hub "logits-processor", Ops "sample" and "How it works";
 // unsatisfiable rows as in TensorRT-Edge-LLM "Guided Decoder").
 //
-// GB300 design.  One row is owned by a thread-block cluster of C CTAs (C in
-// {1, 2, 4, 8}); each CTA stages its contiguous chunk of the row (and of the
-// row's bitmask) in shared memory with cp.async, so HBM is read exactly once and
-// every later pass runs on chip.  The CTAs combine partial results through
-// distributed shared memory (DSMEM) behind hardware cluster barriers -- no global
-// scratch, no atomics on global memory, no spin-waits.
+// GB300 design: one streaming pass over HBM through the Tensor Memory
+// Accelerator.  A row is split over a thread-block cluster of S CTAs (S = 1 for
+// big batches).  Each CTA streams its part of the row through a ring of four
+// 8 KB shared-memory stages: one thread keeps bulk copies (cp.async.bulk, with
+// the stage's bitmask words) in flight on mbarriers, the 256 threads consume
+// each landed stage from shared memory.  Three CTAs share an SM, so many rows'
+// reduction chains are in flight at once.  The CTAs of a row combine partial
+// results through distributed shared memory (DSMEM) behind cluster barriers;
+// nothing is written to global memory but the ids.
 //
-// Per row:
-//   P1  candidate max / argmax / count (overlapped with the staged loads);
-//       cluster reduce.  No candidate -> -1; greedy -> argmax.
-//   P2  (top-p only) S = sum of exp((x - max) / T) over candidates.
-//   cut a lower bound on the final keep-threshold from whichever filter can
-//       certify one: min-p exactly, top-k from the k-th largest per-thread
-//       maximum, top-p from the tail-mass bound (candidates below the cut carry
-//       at most (1 - top_p) S); candidates at or above it are compacted (P3) into
-//       a per-CTA buffer.
-//   sel the keep-threshold max(t_k, t_p, t_m) by an MSD radix select over the
-//       order-preserving key of the logit (counts for top-k, fixed-point softmax
-//       mass for top-p, summed across the cluster per digit).  Top-k and top-p
-//       share one descent: the threshold is the largest key at which either
-//       "count >= k" or "mass >= top_p * S" first holds.  The descent runs over
-//       the compacted buffers; if they overflowed or do not reach the threshold
-//       it runs again over the staged chunks (exact in every case).
-//   draw Gumbel-max over the kept set with Philox4x32-10 noise keyed by
-//       (seed, row, offset); rows without filters draw over all candidates that
-//       can still win (z >= z_max - (g_max - g_min)), pruning any token whose best
-//       possible score is below the running best.
-// Masses are 2^-40 fixed point in 64-bit integers, so every sum is exact and
-// order-independent: results are deterministic in (seed, offset).
+// Per row, in the stream:
+//   * candidate max, the vector holding it (its lowest index is found after the
+//     pass), the candidate count and, for top-p rows, an online softmax sum;
+//   * filtered rows: every candidate within a window below the running maximum
+//     (shared by the CTA's warps through a shared-memory atomicMax) is appended
+//     to a compaction buffer.  The window is exactly the min-p bound when min-p is
+//     on (max + T ln min_p); otherwise a number of temperature units growing with
+//     ln(1 / (1 - top_p)) for top-p and a fixed number of logits for top-k.  The
+//     running maximum never exceeds the row maximum, so the buffer holds every
+//     candidate in [max - window, max];
+//   * rows without filters draw Gumbel-max directly (no threshold needed),
+//     skipping any token whose best possible score is below the running best.
+// After the stream (one exchange): no candidate -> -1; greedy -> argmax;
+// unfiltered -> the best score's token.  Filtered rows find the keep-threshold
+// max(t_k, t_p, t_m) by an MSD radix select over the order-preserving key of the
+// logit -- counts for top-k and 2^-40 fixed-point softmax mass for top-p, pre-summed
+// per warp (match_any + redux) and summed over the cluster per digit; one descent
+// serves both filters: the threshold is the largest key at which "count >= k" or
+// "mass >= top_p S" first holds.  The descent runs on the buffer, counting only the
+// region where the buffer is complete; if the threshold is not found there (or a
+// buffer overflowed) the CTAs stream their parts again (an L2 hit in practice) and
+// select and draw from those.  The draw is Gumbel-max over the kept set with
+// Philox4x32-10 noise keyed by (seed, row, offset).
+// Masses are integers, so every cluster-wide sum is exact and order-independent;
+// the softmax sum is reduced in a fixed order.  Results are deterministic in
+// (seed, offset).
 #include <cooperative_groups.h>
 
 #include <algorithm>
 #include <climits>
 #include <cmath>
+#include <map>
 #include <mutex>
 
 #include "common.cuh"
@@ -47,13 +55,18 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kStages = 4;
-constexpr int kKBins = 128;             // log-spaced bins of (max - thread max)
-constexpr int kKBase = (127 - 6) << 3;  // code of 2^-6 (8 exponent + 3 fraction bits)
-constexpr int kMaxCluster = 8;
-constexpr int kDefaultCap = 4096;
+constexpr int kRing = 4;                 // stages in flight per CTA
+constexpr int kPieceBytes = 8192;        // bytes of logits per stage
+constexpr int kPieceWords = kPieceBytes / 2 / 32 + 2;  // bitmask words a stage can need
+constexpr int kMaskSlot = (16 + 4 * kPieceWords + 15) / 16 * 16;
+constexpr int kKBins = 128;              // log-spaced bins of (row max - thread max)
+constexpr int kKBase = (127 - 6) << 3;   // code of 2^-6 (8 exponent + 3 fraction bits)
+constexpr int kMaxSplit = 16;
+constexpr int kCap = 3072;               // compaction entries per CTA
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr double kFix = 1099511627776.0;  // 2^40
+constexpr float kWindowK = 6.f;          // top-k window, in logits
+constexpr int kSmem = kRing * kPieceBytes + kRing * kMaskSlot + kCap * 8;
+constexpr uint32_t kMaxWaitTries = 1u << 22;
 
 struct SampleArgs {
   const char* logits;
@@ -75,25 +88,21 @@ struct SampleArgs {
   float minp_s;
   uint64_t seed, offset;
   int64_t* out;
-  int chunk;   // tokens per CTA (multiple of 32)
-  int cap;     // compaction buffer entries per CTA
-  int mw_off;  // byte offset of the staged bitmask words in dynamic shared memory
-  int buf_off; // byte offset of the compaction buffer
+  int chunk;  // tokens per CTA (a multiple of 32)
 };
 
 struct Xchg {  // per-CTA values read by the other CTAs of the cluster
   float max;
   int arg;
+  float sum;  // softmax sum relative to max
   int ncand;
-  float sum;
-  int count;
   int overflow;
+  int err;
   float best;
   int best_v;
-  unsigned kcnt[kKBins];
 };
 
-struct Hist {  // double-buffered radix histograms
+struct Hist {  // radix histograms, double-buffered by pass parity
   unsigned long long mass[2][256];
   unsigned cnt[2][256];
 };
@@ -105,49 +114,23 @@ __device__ __forceinline__ void arg_combine(float& s, int& v, float s2, int v2) 
   }
 }
 
-__device__ __forceinline__ void warp_argmax(float& s, int& v) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    const float s2 = __shfl_xor_sync(kFullWarp, s, o);
-    const int v2 = __shfl_xor_sync(kFullWarp, v, o);
-    arg_combine(s, v, s2, v2);
+// Merge two partial row summaries (max, lowest index of the max and -- when
+// with_sum -- the sum of exp2((x - max) c2)).  Symmetric in its two arguments, so
+// a butterfly leaves the same value in every lane and any fixed merge order is
+// deterministic.
+__device__ __forceinline__ void row_combine(float& m, int& v, float& s, float m2, int v2, float s2,
+                                            float c2, bool with_sum) {
+  if (with_sum) {
+    const float M = fmaxf(m, m2);
+    const float a = m > -INFINITY ? s * exp2f((m - M) * c2) : 0.f;
+    const float b = m2 > -INFINITY ? s2 * exp2f((m2 - M) * c2) : 0.f;
+    s = a + b;
   }
+  arg_combine(m, v, m2, v2);
 }
 
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(kFullWarp, x, o);
-  return x;
-}
-
-__device__ __forceinline__ int warp_sum_i(int x) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(kFullWarp, x, o);
-  return x;
-}
-
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;\n" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_dyn(int n) {
-  switch (n) {
-    case 0: cp_async_wait<0>(); break;
-    case 1: cp_async_wait<1>(); break;
-    case 2: cp_async_wait<2>(); break;
-    default: cp_async_wait<3>(); break;
-  }
-}
-
-// Log-spaced bin of d >= 0: bin 0 holds d < 2^-6, bin j >= 1 holds d in
-// [2^-6 ... ) with 8 bins per octave; the last bin also holds everything larger.
+// Log-spaced bin of d >= 0: bin 0 holds d < 2^-6, then 8 bins per octave; the
+// last bin also takes everything larger.
 __device__ __forceinline__ int kbin(float d) {
   const int code = int(__float_as_uint(d) >> 20);
   return min(max(code - kKBase + 1, 0), kKBins - 1);
@@ -157,71 +140,209 @@ __device__ __forceinline__ float kbin_hi(int j) {
   return j == 0 ? 0.015625f : __uint_as_float(unsigned(j + kKBase) << 20);
 }
 
-// Per-CTA view of the staged chunk: token v = start + i for local element i.
+// ------------------------------------------------------ TMA and mbarriers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* m, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(m)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+// Arrive once and add `bytes` to the phase's expected transaction count.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* m, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(m)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* m, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(m)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase of the given parity to complete.  Each try_wait
+// suspends the thread for a hardware-chosen time slice; after kMaxWaitTries
+// failures (far beyond any copy's latency) it gives up and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t* m, uint32_t parity) {
+  for (uint32_t i = 0; i < kMaxWaitTries; ++i)
+    if (mbar_try_wait(m, parity)) return true;
+  return false;
+}
+// One-dimensional bulk copy global -> shared completing on mbarrier m; both
+// addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* m) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(m))
+      : "memory");
+}
+
+// ------------------------------------------------------------ row part
+
+// One CTA's part of one row: local element i is token start + i, at byte
+// mis + i * EB of a 16-byte aligned window starting at g0.  The window is
+// streamed in pieces of kPieceBytes.  Whole 16-byte vectors [qf0, qf1) of the
+// window arrive by bulk copy; the ragged first and last vectors are read from
+// global memory when used.  Each piece's bitmask words arrive with it: words
+// [m_lo, m_hi) (relative to the part) sit at byte mmis + 4 (w - m_lo) of the
+// piece's mask slot; other words are read from global memory.
 template <int DT>
-struct Chunk {
+struct Part {
   using E = Elt<DT>;
   static constexpr int EPV = E::kPerVec;
   static constexpr int EB = E::kBytes;
-  const unsigned char* data;  // 16-byte aligned window; element i at byte mis + i*EB
-  const uint32_t* mw;         // staged bitmask words of the chunk
-  int mis, n_local, nvec, nwords, start;
+  static constexpr uint32_t ALL = (1u << EPV) - 1u;
+  const char* g0;
+  const uint32_t* gmask;  // the part's bitmask words (masked rows)
+  int start, n_local, mis, win, nvec, nwords, qf0, qf1, npieces;
   bool masked;
 
-  // candidate bits of vector q: element e is a token of this chunk and kept by the mask
-  __device__ __forceinline__ uint32_t bits(int q, int& i0) const {
-    i0 = (16 * q - mis) / EB;
-    const int lo = i0 < 0 ? -i0 : 0;
-    const int hi = min(EPV, n_local - i0);
-    uint32_t valid = hi > lo ? (((1u << hi) - 1u) & ~((1u << lo) - 1u)) : 0u;
-    if (!masked || !valid) return valid;
-    const int w = i0 >> 5;  // floor division, -1 for a negative i0
-    const int sh = i0 & 31;
-    const uint32_t w0 = w >= 0 ? mw[w] : 0u;
-    const uint32_t w1 = (sh + EPV > 32 && w + 1 < nwords) ? mw[w + 1] : 0u;
-    const uint32_t m = uint32_t(((uint64_t(w1) << 32) | w0) >> sh);
-    return valid & m;
+  __device__ __forceinline__ void init(const SampleArgs& a, int row, int rank, bool m) {
+    start = rank * a.chunk;
+    n_local = max(0, min(a.chunk, a.V - start));
+    const char* gsrc = a.logits + int64_t(row) * a.stride_bytes + int64_t(start) * EB;
+    mis = int(reinterpret_cast<uintptr_t>(gsrc) & 15);
+    g0 = gsrc - mis;
+    win = mis + n_local * EB;
+    nvec = n_local ? (win + 15) >> 4 : 0;
+    qf0 = (mis + 15) >> 4;
+    qf1 = win >> 4;
+    nwords = (n_local + 31) >> 5;
+    npieces = n_local ? (win + kPieceBytes - 1) / kPieceBytes : 0;
+    masked = m;
+    gmask = m ? a.bitmask + int64_t(row) * a.bm_stride + (start >> 5) : nullptr;
   }
-  __device__ __forceinline__ uint4 vec(int q) const {
-    return *reinterpret_cast<const uint4*>(data + 16 * q);
+  // vectors [q0, q1) of piece j
+  __device__ __forceinline__ void piece_vecs(int j, int& q0, int& q1) const {
+    q0 = j * (kPieceBytes / 16);
+    q1 = min(q0 + kPieceBytes / 16, nvec);
+  }
+  // bitmask words [w0, w1) the vectors of piece j touch
+  __device__ __forceinline__ void piece_words(int j, int& w0, int& w1) const {
+    int q0, q1;
+    piece_vecs(j, q0, q1);
+    const int i0 = max((16 * q0 - mis) / EB, 0);
+    const int i1 = min((16 * q1 - mis) / EB, n_local);  // exclusive
+    w0 = i0 >> 5;
+    w1 = i1 > i0 ? ((i1 - 1) >> 5) + 1 : w0;
+  }
+  // the 16-byte aligned interior [m_lo, m_hi) of words [w0, w1), and the byte
+  // offset of word m_lo in its slot
+  __device__ __forceinline__ void mask_interior(int w0, int w1, int& m_lo, int& m_hi,
+                                                int& mmis) const {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(gmask + w0);
+    const int lead = int(((16 - (a0 & 15)) & 15) >> 2);
+    m_lo = min(w0 + lead, w1);
+    const uintptr_t a1 = reinterpret_cast<uintptr_t>(gmask + w1) & ~uintptr_t(15);
+    m_hi = max(m_lo, int((a1 - reinterpret_cast<uintptr_t>(gmask)) >> 2));
+    mmis = 0;
+  }
+  __device__ __forceinline__ uint4 gvec(int q) const {  // from global memory
+    if (q >= qf0 && q < qf1) return __ldg(reinterpret_cast<const uint4*>(g0 + 16 * q));
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) {
+      const int off = 16 * q + e * EB;
+      if (off >= mis && off < win) {
+        const uint32_t b = E::bits1(g0 + off);
+        if (EB == 4)
+          w[e] = b;
+        else
+          w[e >> 1] |= b << (16 * (e & 1));
+      }
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  // candidate bits of vector q (element e a token of this part kept by the mask),
+  // its mask words taken from `mw` (words [m_lo, m_hi)) or global memory
+  __device__ __forceinline__ uint32_t bits(int q, int& i0, const uint32_t* mw, int m_lo,
+                                           int m_hi) const {
+    i0 = (16 * q - mis) / EB;
+    uint32_t valid = ALL;
+    if (i0 < 0 || i0 + EPV > n_local) {
+      const int lo = i0 < 0 ? -i0 : 0;
+      const int hi = min(EPV, n_local - i0);
+      valid = hi > lo ? (((1u << hi) - 1u) & ~((1u << lo) - 1u)) : 0u;
+    }
+    if (!masked || !valid) return valid;
+    const int w = i0 >> 5;  // floor division: -1 for a negative i0
+    const int sh = i0 & 31;
+    auto word = [&](int x) -> uint32_t {
+      return (x >= m_lo && x < m_hi) ? mw[x - m_lo] : __ldg(gmask + x);
+    };
+    const uint32_t w0 = w >= 0 ? word(w) : 0u;
+    const uint32_t w1 = (sh + EPV > 32 && w + 1 < nwords) ? word(w + 1) : 0u;
+    return valid & uint32_t(((uint64_t(w1) << 32) | w0) >> sh);
   }
 };
 
 template <int DT>
-__global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleArgs a) {
   using E = Elt<DT>;
+  using Pt = Part<DT>;
   constexpr int EPV = E::kPerVec;
-  constexpr int EB = E::kBytes;
-  constexpr int kLastShift = E::kLowKeyBit & ~7;
+  constexpr int kLow = int(E::kLowKeyBit);
 
   cg::cluster_group cluster = cg::this_cluster();
   const int C = int(cluster.num_blocks());
   const int rank = int(cluster.block_rank());
-  const int b = int(blockIdx.x) / C;
+  const int row = int(blockIdx.x) / C;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  auto xsync = [&]() {
+    if (C > 1)
+      cluster.sync();
+    else
+      __syncthreads();
+  };
 
   extern __shared__ __align__(16) unsigned char smem[];
-  uint32_t* smw = reinterpret_cast<uint32_t*>(smem + a.mw_off);
-  float* bval = reinterpret_cast<float*>(smem + a.buf_off);
-  int* bidx = reinterpret_cast<int*>(smem + a.buf_off + 4 * a.cap);
+  unsigned char* const ring = smem;
+  unsigned char* const mring = smem + kRing * kPieceBytes;
+  float* const bval = reinterpret_cast<float*>(mring + kRing * kMaskSlot);
+  int* const bidx = reinterpret_cast<int*>(bval + kCap);
 
   __shared__ Xchg xchg;
+  __shared__ float tmaxs[kThreads];
   __shared__ Hist hist;
-  __shared__ float red_f[kWarps];
-  __shared__ int red_i[kWarps];
-  __shared__ int red_n[kWarps];
+  __shared__ float red_f[kWarps], red_s[kWarps], red_b[kWarps];
+  __shared__ int red_i[kWarps], red_n[kWarps], red_bv[kWarps];
   __shared__ unsigned scan_c[kWarps];
   __shared__ unsigned long long scan_m[kWarps];
   __shared__ unsigned kmerge[kKBins];
-  __shared__ int s_count, s_sel;
-  __shared__ unsigned s_above_c;
+  __shared__ int s_count, s_sel, s_err, s_i[4];
+  __shared__ float s_f[2];
+  __shared__ unsigned s_runkey, s_above_c;
   __shared__ unsigned long long s_above_m;
+  __shared__ __align__(8) uint64_t full[kRing];
 
-  // ---------------------------------------------------------------- row setup
-  const float T = a.temp ? a.temp[b] : a.temp_s;
-  int k = a.topk ? a.topk[b] : a.topk_s;
-  const float tp = a.topp ? a.topp[b] : a.topp_s;
-  const float mp = a.minp ? a.minp[b] : a.minp_s;
+  // ------------------------------------------------------------ row set-up
+  const float T = a.temp ? a.temp[row] : a.temp_s;
+  int k = a.topk ? a.topk[row] : a.topk_s;
+  const float tp = a.topp ? a.topp[row] : a.topp_s;
+  const float mp = a.minp ? a.minp[row] : a.minp_s;
+  const bool greedy = !(T > 0.f) || k == 1;
+  const bool has_p = !greedy && tp < 1.f;
+  const bool has_m = !greedy && mp > 0.f;
+  const bool has_k0 = !greedy && k > 0;
+  const bool unfiltered = !greedy && !has_p && !has_m && !has_k0;
+  const bool compact = !greedy && !unfiltered;
+  const float c2 = greedy ? 0.f : kLog2e / T;
+  const float tl = has_m ? T * logf(mp) : 0.f;  // min-p bound below the maximum: max + tl
+  float delta = INFINITY;                       // the compaction window below the running max
+  if (has_m) delta = fminf(delta, -tl);
+  if (has_p) delta = fminf(delta, T * (2.f + 2.5f * logf(1.f / fmaxf(1.f - tp, 1e-6f))));
+  if (has_k0) delta = fminf(delta, kWindowK);
+  if (!(delta > 0.f)) delta = 0.f;
 
   bool masked = false;
   if (a.bitmask) {
@@ -229,463 +350,579 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
       masked = true;
     } else {
       int found = 0;
-      for (int i = tid; i < a.n_indices; i += kThreads) found |= (a.indices[i] == b);
-      masked = __syncthreads_or(found) != 0 && b < a.bm_rows;
+      for (int i = tid; i < a.n_indices; i += kThreads) found |= (a.indices[i] == row);
+      masked = __syncthreads_or(found) != 0 && row < a.bm_rows;
     }
   }
-
-  Chunk<DT> ch;
-  ch.start = rank * a.chunk;
-  ch.n_local = max(0, min(a.chunk, a.V - ch.start));
-  const char* gsrc = a.logits + int64_t(b) * a.stride_bytes + int64_t(ch.start) * EB;
-  ch.mis = int(reinterpret_cast<uintptr_t>(gsrc) & 15);
-  const char* g0 = gsrc - ch.mis;
-  const int win = ch.mis + ch.n_local * EB;
-  ch.nvec = (win + 15) >> 4;
-  ch.nwords = (ch.n_local + 31) >> 5;
-  ch.data = smem;
-  ch.mw = smw;
-  ch.masked = masked;
-
-  if (tid < kKBins) xchg.kcnt[tid] = 0u;
-  if (tid == 0) s_count = 0;
-
-  // staged loads: full 16-byte vectors by cp.async in kStages groups, the ragged
-  // first and last vectors element by element
-  const int qf0 = (ch.mis + 15) >> 4;  // first vector wholly inside the window
-  const int qf1 = win >> 4;            // vectors [qf0, qf1) are whole
-  const int nfull = max(0, qf1 - qf0);
-  if (masked) {
-    const uint32_t* mrow = a.bitmask + int64_t(b) * a.bm_stride + (ch.start >> 5);
-    for (int i = tid; i < ch.nwords; i += kThreads) smw[i] = __ldg(mrow + i);
+  Pt pt;
+  pt.init(a, row, rank, masked);
+  if (tid == 0) {
+    s_count = 0;
+    s_err = 0;
+    s_runkey = fkey(-INFINITY);
+    for (int r = 0; r < kRing; ++r) mbar_init(&full[r], 1);
+    mbar_init_fence();
   }
-  if (ch.n_local > 0) {
-    if (tid < EPV && ch.mis != 0) {  // ragged first vector
-      const int off = tid * EB;
-      if (off >= ch.mis && off < win)
-        E::store1(reinterpret_cast<char*>(smem) + off, E::bits1(g0 + off));
-    }
-    if (tid >= 32 && tid < 32 + EPV && (win & 15) != 0 && qf1 >= qf0) {  // ragged last vector
-      const int off = 16 * qf1 + (tid - 32) * EB;
-      if (off >= ch.mis && off < win)
-        E::store1(reinterpret_cast<char*>(smem) + off, E::bits1(g0 + off));
-    }
-  }
-  for (int s = 0; s < kStages; ++s) {
-    const int lo = qf0 + int(int64_t(nfull) * s / kStages);
-    const int hi = qf0 + int(int64_t(nfull) * (s + 1) / kStages);
-    for (int q = lo + tid; q < hi; q += kThreads) cp_async16(smem + 16 * q, g0 + 16 * q);
-    cp_async_commit();
-  }
+  if (tid < kKBins) kmerge[tid] = 0u;
+  __syncthreads();
 
-  // ------------------------------------------------ P1: max, argmax, count
-  float tmax = -INFINITY;
-  int targ = INT_MAX;
-  int tcnt = 0;
-  auto p1_vec = [&](int q) {
-    int i0;
-    const uint32_t cb = ch.bits(q, i0);
-    if (!cb) return;
-    const uint4 raw = ch.vec(q);
-#pragma unroll
-    for (int e = 0; e < EPV; ++e) {
-      if (!((cb >> e) & 1u)) continue;
-      const float x = E::get(raw, e);
-      if (!(x > -INFINITY)) continue;
-      ++tcnt;
-      const int v = ch.start + i0 + e;
-      if (x > tmax || (x == tmax && v < targ)) {
-        tmax = x;
-        targ = v;
-      }
+  // ------------------------------------------------------------ the ring
+  uint32_t ring_next = 0;  // pieces issued (all passes); slot = n % kRing
+  uint32_t ring_done = 0;  // pieces consumed
+  uint32_t lost = 0;       // bit s: this thread's wait on slot s timed out (parity in bit s + 8)
+  // Thread 0 arms slot (n % kRing) and starts the copies of piece j.
+  auto issue_piece = [&](int j) {
+    const int slot = int(ring_next % kRing);
+    ++ring_next;
+    if (tid != 0) return;
+    int q0, q1;
+    pt.piece_vecs(j, q0, q1);
+    const int v0 = max(q0, pt.qf0), v1 = min(q1, pt.qf1);
+    const uint32_t vbytes = v1 > v0 ? uint32_t(16 * (v1 - v0)) : 0u;
+    uint32_t mbytes = 0;
+    int w0 = 0, w1 = 0, m_lo = 0, m_hi = 0, mmis = 0;
+    if (pt.masked) {
+      pt.piece_words(j, w0, w1);
+      pt.mask_interior(w0, w1, m_lo, m_hi, mmis);
+      mbytes = uint32_t(4 * (m_hi - m_lo));
     }
+    if (s_err) {  // a copy went missing earlier: start no more; the row reports -2
+      mbar_expect_tx(&full[slot], 0);
+      return;
+    }
+    mbar_expect_tx(&full[slot], vbytes + mbytes);
+    if (vbytes)
+      bulk_load(ring + slot * kPieceBytes + 16 * (v0 - q0), pt.g0 + 16 * v0, vbytes, &full[slot]);
+    if (mbytes)
+      bulk_load(mring + slot * kMaskSlot, pt.gmask + m_lo, mbytes, &full[slot]);
   };
-  for (int s = 0; s < kStages; ++s) {
-    cp_async_wait_dyn(kStages - 1 - s);
-    __syncthreads();
-    const int lo = qf0 + int(int64_t(nfull) * s / kStages);
-    const int hi = qf0 + int(int64_t(nfull) * (s + 1) / kStages);
-    for (int q = lo + tid; q < hi; q += kThreads) p1_vec(q);
-    if (s == 0) {  // the ragged vectors, loaded before the first barrier
-      if (tid == 0 && qf0 > 0 && ch.nvec > 0) p1_vec(0);
-      if (tid == 1 && qf1 < ch.nvec && qf1 >= qf0) p1_vec(qf1);
-    }
-  }
-  {
-    float m = tmax;
-    int v = targ;
-    warp_argmax(m, v);
-    const int n = warp_sum_i(tcnt);
-    if (lane == 0) {
-      red_f[warp] = m;
-      red_i[warp] = v;
-      red_n[warp] = n;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      float bm = -INFINITY;
-      int bv = INT_MAX, nn = 0;
-      for (int w = 0; w < kWarps; ++w) {
-        arg_combine(bm, bv, red_f[w], red_i[w]);
-        nn += red_n[w];
+  // Streams the part once: f(q, valid, raw, cb, i0) for every vector q, in
+  // warp-uniform iterations (valid false on padding lanes); after each
+  // iteration, g() (also warp-uniform).  Returns false if a stage never landed.
+  auto stream = [&](auto&& f, auto&& g) {
+    const int np = pt.npieces;
+    for (int j = 0; j < min(np, kRing); ++j) issue_piece(j);
+    bool ok = true;
+    for (int j = 0; j < np; ++j) {
+      const int slot = int(ring_done % kRing);
+      const uint32_t parity = (ring_done / kRing) & 1u;
+      ++ring_done;
+      if (!mbar_wait(&full[slot], parity)) {
+        ok = false;
+        s_err = 1;
+        lost |= (1u << slot) | (parity << (slot + 8));
       }
-      xchg.max = bm;
-      xchg.arg = bv;
-      xchg.ncand = nn;
+      int q0, q1, w0 = 0, w1 = 0, m_lo = 0, m_hi = 0, mmis = 0;
+      pt.piece_vecs(j, q0, q1);
+      if (pt.masked) {
+        pt.piece_words(j, w0, w1);
+        pt.mask_interior(w0, w1, m_lo, m_hi, mmis);
+      }
+      const unsigned char* data = ring + slot * kPieceBytes;
+      const uint32_t* mw = reinterpret_cast<const uint32_t*>(mring + slot * kMaskSlot);
+      for (int base = q0; base < q1; base += kThreads) {
+        const int q = base + tid;
+        const bool valid = q < q1;
+        int i0 = 0;
+        uint32_t cb = 0;
+        uint4 raw = make_uint4(0, 0, 0, 0);
+        if (valid) {
+          cb = pt.bits(q, i0, mw, m_lo, m_hi);
+          if (cb)
+            raw = (q >= pt.qf0 && q < pt.qf1)
+                      ? *reinterpret_cast<const uint4*>(data + 16 * (q - q0))
+                      : pt.gvec(q);
+        }
+        f(q, valid, raw, cb, i0);
+        g();
+      }
+      __syncthreads();  // every thread is done with the slot
+      if (j + kRing < np) issue_piece(j + kRing);
     }
-  }
-  cluster.sync();  // #1
+    return ok;
+  };
 
-  float lmax = -INFINITY;
-  int larg = INT_MAX;
-  int ncand = 0;
-  for (int r = 0; r < C; ++r) {
-    const Xchg* p = cluster.map_shared_rank(&xchg, r);
-    arg_combine(lmax, larg, p->max, p->arg);
-    ncand += p->ncand;
-  }
-
-  const bool greedy = !(T > 0.f) || k == 1;
-  if (ncand == 0 || greedy) {
-    if (rank == 0 && tid == 0) a.out[b] = ncand == 0 ? -1 : larg;
-    cluster.sync();
-    return;
-  }
-
-  // ------------------------------------------------------------ row constants
-  if (k > 0 && k >= ncand) k = 0;  // keeps every candidate
-  const bool has_k = k > 0;
-  const bool has_p = tp < 1.f;
-  const bool has_m = mp > 0.f;
-  const float c2 = kLog2e / T;
-  float fm = -INFINITY;  // min-p: keep x >= fm
-  if (has_m) {
-    const double lm = double(lmax) + double(T) * log(double(mp));
-    fm = fminf(__double2float_ru(lm), lmax);
-  }
-
-  float best = -INFINITY;
-  int bestv = INT_MAX;
   const uint2 key = make_uint2(uint32_t(a.seed), uint32_t(a.seed >> 32));
-  auto score_of = [&](float x, int v, uint4& w4, int& wgrp) {
+  // Gumbel score of candidate (z = x / T, token v); w4/wgrp cache v's Philox block
+  auto score_of = [&](float z, int v, uint4& w4, int& wgrp) {
     const int grp = v >> 2;
     if (grp != wgrp) {
-      w4 = philox4x32_10(make_uint4(uint32_t(grp), uint32_t(b), uint32_t(a.offset),
+      w4 = philox4x32_10(make_uint4(uint32_t(grp), uint32_t(row), uint32_t(a.offset),
                                     uint32_t(a.offset >> 32)),
                          key);
       wgrp = grp;
     }
     const uint32_t word = (v & 3) == 0 ? w4.x : (v & 3) == 1 ? w4.y : (v & 3) == 2 ? w4.z : w4.w;
-    return __fdiv_rn(x, T) + gumbel_from_word(word);
-  };
-  // Gumbel-max over the candidates of the staged chunk with x >= lo
-  auto draw_chunk = [&](float lo) {
-    uint4 w4 = make_uint4(0, 0, 0, 0);
-    int wgrp = -1;
-    for (int q = tid; q < ch.nvec; q += kThreads) {
-      int i0;
-      const uint32_t cb = ch.bits(q, i0);
-      if (!cb) continue;
-      const uint4 raw = ch.vec(q);
-#pragma unroll
-      for (int e = 0; e < EPV; ++e) {
-        if (!((cb >> e) & 1u)) continue;
-        const float x = E::get(raw, e);
-        if (!(x >= lo) || !(x > -INFINITY)) continue;
-        const float z = __fdiv_rn(x, T);
-        if (z + kGumbelMax < best) continue;  // cannot beat this thread's best
-        const int v = ch.start + i0 + e;
-        arg_combine(best, bestv, score_of(x, v, w4, wgrp), v);
-      }
-    }
-  };
-  // Gumbel-max over the compacted buffer entries with x >= lo
-  auto draw_buffer = [&](float lo, int n) {
-    for (int i = tid; i < n; i += kThreads) {
-      const float x = bval[i];
-      if (!(x >= lo)) continue;
-      uint4 w4;
-      int wgrp = -1;
-      const int v = bidx[i];
-      arg_combine(best, bestv, score_of(x, v, w4, wgrp), v);
-    }
-  };
-  // block + cluster argmax of (best, bestv); rank 0 writes the id
-  auto finish_draw = [&]() {
-    float m = best;
-    int v = bestv;
-    warp_argmax(m, v);
-    if (lane == 0) {
-      red_f[warp] = m;
-      red_i[warp] = v;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      float bm = -INFINITY;
-      int bv = INT_MAX;
-      for (int w = 0; w < kWarps; ++w) arg_combine(bm, bv, red_f[w], red_i[w]);
-      xchg.best = bm;
-      xchg.best_v = bv;
-    }
-    cluster.sync();
-    if (rank == 0 && tid == 0) {
-      float bm = -INFINITY;
-      int bv = INT_MAX;
-      for (int r = 0; r < C; ++r) {
-        const Xchg* p = cluster.map_shared_rank(&xchg, r);
-        arg_combine(bm, bv, p->best, p->best_v);
-      }
-      a.out[b] = bv == INT_MAX ? -1 : bv;
-    }
-    cluster.sync();
+    return z + gumbel_from_word(word);
   };
 
-  if (!has_k && !has_p && !has_m) {  // unfiltered: one Gumbel-max pass
-    const double lo = double(lmax) - double(T) * double(kGumbelMax - kGumbelMin);
-    draw_chunk(__double2float_rd(lo));
-    finish_draw();
+  // -------------------------------------------------------------- stream
+  float m = -INFINITY, sm = 0.f;  // running max and softmax sum relative to it
+  int mq = -1, cnt = 0;           // vector of the running max; candidate bits seen
+  float best = -INFINITY;         // unfiltered rows: running best score
+  int bestv = INT_MAX;
+  uint4 w4 = make_uint4(0, 0, 0, 0);
+  int wgrp = -1;
+  // this iteration's vector (kept for the compaction step that follows it)
+  uint4 it_raw = make_uint4(0, 0, 0, 0);
+  uint32_t it_cb = 0;
+  int it_i0 = 0;
+  float it_vm = -INFINITY;
+  auto on_vec = [&](int q, bool valid, const uint4& raw, uint32_t cb, int i0) {
+    it_raw = raw;
+    it_cb = cb;
+    it_i0 = i0;
+    it_vm = -INFINITY;
+    if (!cb) return;
+    cnt += __popc(cb);
+    float xs[EPV];
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) {
+      xs[e] = ((cb >> e) & 1u) ? E::get(raw, e) : -INFINITY;
+      it_vm = fmaxf(it_vm, xs[e]);
+    }
+    if (it_vm > m) {
+      if (has_p && m > -INFINITY) sm *= exp2f((m - it_vm) * c2);
+      m = it_vm;
+      mq = q;
+    }
+    if (has_p) {
+      const float off = m * c2;
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) sm += exp2f(fmaf(xs[e], c2, -off));
+    }
+    if (unfiltered) {
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        if (!(xs[e] > -INFINITY)) continue;
+        const float z = __fdiv_rn(xs[e], T);
+        if (z + kGumbelMax < best) continue;  // cannot win
+        const int v = pt.start + i0 + e;
+        arg_combine(best, bestv, score_of(z, v, w4, wgrp), v);
+      }
+    }
+  };
+  // filtered rows: append this iteration's candidates within the window
+  auto on_iter = [&]() {
+    if (!compact) return;
+    float wm = m;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(kFullWarp, wm, o));
+    if (lane == 0 && wm > -INFINITY) atomicMax(&s_runkey, fkey(wm));
+    const float rm = fmaxf(wm, key_float(*(volatile unsigned*)&s_runkey));
+    const float cut = __fsub_rd(rm, delta);
+    if (!__any_sync(kFullWarp, it_vm >= cut)) return;
+    uint32_t pass = 0;
+    if (it_vm >= cut) {
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        const float x = E::get(it_raw, e);
+        if (((it_cb >> e) & 1u) && x >= cut && x > -INFINITY) pass |= 1u << e;
+      }
+    }
+    const int n = __popc(pass);
+    int incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFullWarp, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int pos = 0;
+    if (lane == 31) pos = atomicAdd(&s_count, incl);
+    pos = __shfl_sync(kFullWarp, pos, 31) + incl - n;
+    while (pass) {
+      const int e = __ffs(pass) - 1;
+      pass &= pass - 1;
+      if (pos < kCap) {
+        bval[pos] = E::get(it_raw, e);
+        bidx[pos] = pt.start + it_i0 + e;
+      }
+      ++pos;
+    }
+  };
+  const bool stream_ok = stream(on_vec, on_iter);
+
+  // ------------------------------------------------------ row summaries
+  tmaxs[tid] = m;
+  int targ = INT_MAX;
+  if (mq >= 0) {  // lowest index of the thread's maximum, in the first vector holding it
+    int i0;
+    const uint32_t cb = pt.bits(mq, i0, nullptr, 0, 0);
+    const uint4 raw = pt.gvec(mq);
+#pragma unroll
+    for (int e = EPV - 1; e >= 0; --e)
+      if (((cb >> e) & 1u) && E::get(raw, e) == m) targ = pt.start + i0 + e;
+  }
+  {
+    float wm = m, ws = sm, wb = best;
+    int wv = targ, wn = cnt, wbv = bestv;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float m2 = __shfl_xor_sync(kFullWarp, wm, o);
+      const float s2 = __shfl_xor_sync(kFullWarp, ws, o);
+      const int v2 = __shfl_xor_sync(kFullWarp, wv, o);
+      wn += __shfl_xor_sync(kFullWarp, wn, o);
+      row_combine(wm, wv, ws, m2, v2, s2, c2, has_p);
+      if (unfiltered) {
+        const float b2 = __shfl_xor_sync(kFullWarp, wb, o);
+        const int bv2 = __shfl_xor_sync(kFullWarp, wbv, o);
+        arg_combine(wb, wbv, b2, bv2);
+      }
+    }
+    if (lane == 0) {
+      red_f[warp] = wm;
+      red_s[warp] = ws;
+      red_i[warp] = wv;
+      red_n[warp] = wn;
+      red_b[warp] = wb;
+      red_bv[warp] = wbv;
+    }
+  }
+  const int cta_err = __syncthreads_or(!stream_ok);
+  if (warp == 0) {
+    float wm = -INFINITY, ws = 0.f, wb = -INFINITY;
+    int wv = INT_MAX, wn = 0, wbv = INT_MAX;
+    if (lane < kWarps) {
+      wm = red_f[lane];
+      ws = red_s[lane];
+      wv = red_i[lane];
+      wn = red_n[lane];
+      wb = red_b[lane];
+      wbv = red_bv[lane];
+    }
+#pragma unroll
+    for (int o = 4; o; o >>= 1) {
+      const float m2 = __shfl_xor_sync(kFullWarp, wm, o);
+      const float s2 = __shfl_xor_sync(kFullWarp, ws, o);
+      const int v2 = __shfl_xor_sync(kFullWarp, wv, o);
+      wn += __shfl_xor_sync(kFullWarp, wn, o);
+      row_combine(wm, wv, ws, m2, v2, s2, c2, has_p);
+      const float b2 = __shfl_xor_sync(kFullWarp, wb, o);
+      const int bv2 = __shfl_xor_sync(kFullWarp, wbv, o);
+      arg_combine(wb, wbv, b2, bv2);
+    }
+    if (lane == 0) {
+      xchg.max = wm;
+      xchg.arg = wv;
+      xchg.sum = ws;
+      xchg.ncand = wn;
+      xchg.best = wb;
+      xchg.best_v = wbv;
+      xchg.overflow = s_count > kCap;
+      xchg.err = cta_err;
+    }
+  }
+  xsync();  // #1: every CTA's summary is visible to its cluster
+  if (warp == 0) {
+    float wm = -INFINITY, ws = 0.f, wb = -INFINITY;
+    int wv = INT_MAX, wn = 0, wbv = INT_MAX, ov = 0, er = 0;
+    if (lane < C) {
+      const Xchg* p = cluster.map_shared_rank(&xchg, lane);
+      wm = p->max;
+      wv = p->arg;
+      ws = p->sum;
+      wn = p->ncand;
+      wb = p->best;
+      wbv = p->best_v;
+      ov = p->overflow;
+      er = p->err;
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float m2 = __shfl_xor_sync(kFullWarp, wm, o);
+      const float s2 = __shfl_xor_sync(kFullWarp, ws, o);
+      const int v2 = __shfl_xor_sync(kFullWarp, wv, o);
+      wn += __shfl_xor_sync(kFullWarp, wn, o);
+      row_combine(wm, wv, ws, m2, v2, s2, c2, has_p);
+      const float b2 = __shfl_xor_sync(kFullWarp, wb, o);
+      const int bv2 = __shfl_xor_sync(kFullWarp, wbv, o);
+      arg_combine(wb, wbv, b2, bv2);
+    }
+    ov = __any_sync(kFullWarp, ov != 0);
+    er = __any_sync(kFullWarp, er != 0);
+    if (lane == 0) {
+      s_f[0] = wm;
+      s_f[1] = ws;
+      s_i[0] = wv;
+      s_i[1] = wn;
+      s_i[2] = wbv;
+      s_i[3] = ov | (er << 1);
+    }
+  }
+  __syncthreads();
+  const float lmax = s_f[0];
+  const float S = s_f[1];
+  const int larg = s_i[0];
+  const int ncand_ub = s_i[1];  // candidates counted by their bits (-inf included)
+  const bool row_err = (s_i[3] >> 1) != 0;
+
+  // a CTA leaves only once its ring is idle and its peers are done reading it:
+  // a stage whose wait timed out gets one more bounded wait for its copies
+  auto leave = [&]() {
+    for (int sl = 0; sl < kRing; ++sl)
+      if ((lost >> sl) & 1u) (void)mbar_wait(&full[sl], (lost >> (sl + 8)) & 1u);
+    if (C > 1) cluster.sync();
+  };
+  if (row_err || lmax == -INFINITY || greedy || unfiltered) {
+    if (rank == 0 && tid == 0)
+      a.out[row] = row_err ? -2
+                   : lmax == -INFINITY ? -1
+                   : greedy ? larg
+                            : (s_i[2] == INT_MAX ? -1 : s_i[2]);
+    leave();
     return;
   }
+  const bool any_overflow = (s_i[3] & 1) != 0;
+  const int nbuf = min(s_count, kCap);
 
-  // ------------------------------------------------------------ P2: softmax sum
-  float S = 0.f;
+  // --------------------------------------------------------- filter bounds
+  if (k > 0 && k >= ncand_ub) k = 0;  // keeps every candidate
+  const bool has_k = k > 0;
+  const float fm = has_m ? fminf(__fadd_ru(lmax, tl), lmax) : -INFINITY;
+  // top-k: the k-th largest per-thread maximum of the cluster bounds t_k from below
+  int jk = -1;
+  if (has_k && k <= C * kThreads) {
+    for (int r = 0; r < C; ++r) {
+      const float v = cluster.map_shared_rank(&tmaxs[0], r)[tid];
+      if (v > -INFINITY) atomicAdd(&kmerge[kbin(lmax - v)], 1u);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const unsigned c0 = kmerge[4 * lane], c1 = kmerge[4 * lane + 1];
+      const unsigned cc2 = kmerge[4 * lane + 2], c3 = kmerge[4 * lane + 3];
+      unsigned incl = c0 + c1 + cc2 + c3;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(kFullWarp, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned excl = incl - (c0 + c1 + cc2 + c3);
+      const unsigned kk = unsigned(k);
+      int j = -1;
+      if (excl < kk && incl >= kk) {
+        unsigned cum = excl + c0;
+        j = cum >= kk ? 4 * lane
+                      : ((cum += c1) >= kk ? 4 * lane + 1
+                                           : ((cum += cc2) >= kk ? 4 * lane + 2 : 4 * lane + 3));
+      }
+      const unsigned found = __ballot_sync(kFullWarp, j >= 0);
+      j = __shfl_sync(kFullWarp, j, found ? __ffs(found) - 1 : 0);
+      if (lane == 0) s_i[2] = found ? j : -1;
+    }
+    __syncthreads();
+    jk = s_i[2];
+  }
+  float fcut = fm;  // certified lower bound of the keep-threshold
+  if (jk >= 0 && jk < kKBins - 1) fcut = fmaxf(fcut, __fsub_rd(lmax, kbin_hi(jk)));
   if (has_p) {
-    float ts = 0.f;
-    for (int q = tid; q < ch.nvec; q += kThreads) {
-      int i0;
-      const uint32_t cb = ch.bits(q, i0);
-      if (!cb) continue;
-      const uint4 raw = ch.vec(q);
-#pragma unroll
-      for (int e = 0; e < EPV; ++e) {
-        if (!((cb >> e) & 1u)) continue;
-        const float x = E::get(raw, e);
-        if (x > -INFINITY) ts += exp2f((x - lmax) * c2);
-      }
-    }
-    ts = warp_sum(ts);
-    if (lane == 0) red_f[warp] = ts;
+    float D = logf(float(ncand_ub) / (fmaxf(1.f - tp, 1e-30f) * S));
+    D = fmaxf(D, 0.f) * 1.001f + 1e-3f;
+    fcut = fmaxf(fcut, __fsub_rd(lmax, T * D));
   }
-  const bool kbound = has_k && k <= C * kThreads;
-  if (kbound && tmax > -INFINITY) atomicAdd(&xchg.kcnt[kbin(lmax - tmax)], 1u);
-  __syncthreads();
-  if (has_p && tid == 0) {
-    float t = 0.f;
-    for (int w = 0; w < kWarps; ++w) t += red_f[w];
-    xchg.sum = t;
-  }
-  cluster.sync();  // #2
-  if (has_p)
-    for (int r = 0; r < C; ++r) S += cluster.map_shared_rank(&xchg, r)->sum;
-  if (kbound && tid < kKBins) {
-    unsigned m = 0;
-    for (int r = 0; r < C; ++r) m += cluster.map_shared_rank(&xchg, r)->kcnt[tid];
-    kmerge[tid] = m;
-  }
-  __syncthreads();
+  // the buffer holds every candidate in [lo_w, lmax]
+  const float lo_w = has_m ? fm : __fsub_ru(lmax, delta);
 
-  // --------------------------------------------------- cut (certified bound)
-  double cut = -INFINITY;
-  if (has_m) cut = fmax(cut, double(fm));
-  if (kbound) {
-    unsigned cum = 0;
-    int jk = -1;
-    for (int j = 0; j < kKBins - 1; ++j) {
-      cum += kmerge[j];
-      if (cum >= unsigned(k)) {
-        jk = j;
-        break;
-      }
-    }
-    if (jk >= 0) cut = fmax(cut, double(lmax) - double(kbin_hi(jk)));
-  }
-  if (has_p) {
-    double D = log(double(ncand) / (fmax(1.0 - double(tp), 1e-30) * double(S)));
-    D = fmax(D, 0.0) * 1.0001 + 1e-4;
-    cut = fmax(cut, double(lmax) - double(T) * D);
-  }
-  const float fcut = cut == -INFINITY ? -INFINITY : __double2float_rd(cut);
-
-  // ------------------------------------------ P3: compact candidates >= cut
-  {
-    const int iters = (ch.nvec + kThreads - 1) / kThreads;
-    for (int it = 0; it < iters; ++it) {
-      const int q = it * kThreads + tid;
-      uint32_t pass = 0;
-      int i0 = 0;
-      uint4 raw = make_uint4(0, 0, 0, 0);
-      if (q < ch.nvec) {
-        const uint32_t cb = ch.bits(q, i0);
-        if (cb) {
-          raw = ch.vec(q);
-#pragma unroll
-          for (int e = 0; e < EPV; ++e) {
-            if (!((cb >> e) & 1u)) continue;
-            const float x = E::get(raw, e);
-            if (x >= fcut && x > -INFINITY) pass |= 1u << e;
-          }
-        }
-      }
-      const int n = __popc(pass);
-      if (__any_sync(kFullWarp, n != 0)) {
-        int incl = n;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(kFullWarp, incl, o);
-          if (lane >= o) incl += y;
-        }
-        int base = 0;
-        if (lane == 31) base = atomicAdd(&s_count, incl);
-        base = __shfl_sync(kFullWarp, base, 31);
-        int pos = base + incl - n;
-        while (pass) {
-          const int e = __ffs(pass) - 1;
-          pass &= pass - 1;
-          if (pos < a.cap) {
-            bval[pos] = E::get(raw, e);
-            bidx[pos] = ch.start + i0 + e;
-          }
-          ++pos;
-        }
-      }
-    }
-  }
-  __syncthreads();
-  if (tid == 0) {
-    xchg.count = min(s_count, a.cap);
-    xchg.overflow = s_count > a.cap;
-  }
-  cluster.sync();  // #3
-  int any_overflow = 0;
-  for (int r = 0; r < C; ++r) any_overflow |= cluster.map_shared_rank(&xchg, r)->overflow;
-  const int nbuf = xchg.count;
-
-  // -------------------------------------- radix select of the keep-threshold
+  // ------------------------------------ radix select of the threshold
   unsigned long long P = 0ull;  // fixed-point top-p mass target
   if (has_p) {
-    const double t = fmax(double(tp), 0.0) * double(S) * kFix;
-    P = t >= 1.8e19 ? ~0ull : static_cast<unsigned long long>(t);
+    const float t = fmaxf(tp, 0.f) * S * 1099511627776.0f;
+    P = t >= 1.8e19f ? ~0ull : static_cast<unsigned long long>(t);
   }
   int npass = 0;
-  // Finds the largest key x >= key(lo) with count(>= x) >= k (top-k) or
-  // mass(>= x) >= P (top-p).  Returns false when no such key exists.
+  // Largest key x >= key(lo) with count(>= x) >= k (top-k) or mass(>= x) >= P
+  // (top-p), counting candidates of the buffer or of a fresh stream of the part.
+  // False when none exists.
   auto descend = [&](bool from_buffer, float lo, uint32_t& out_key) -> bool {
     const uint32_t klo = fkey(lo), khi = fkey(lmax);
     const uint32_t diff = klo ^ khi;
-    const int hb = diff ? 31 - __clz(diff) : int(E::kLowKeyBit);
-    int shift = max(hb - 7, 0);
-    shift = max(shift & ~7, kLastShift);  // 8-bit digits aligned to the byte grid
-    if (hb >= shift + 8) shift += 8;      // keep the highest differing bit inside
-    uint32_t prefix = shift + 8 >= 32 ? 0u : (khi >> (shift + 8)) << (shift + 8);
+    int top = diff ? 32 - __clz(diff) : kLow + 1;  // one past the highest differing bit
+    top = max(top, kLow + 1);
+    int shift = max(top - 8, kLow);
+    uint32_t prefix = top >= 32 ? 0u : khi & ~((1u << top) - 1u);
     unsigned above_c = 0;
     unsigned long long above_m = 0;
     for (;;) {
-      const int par = npass & 1;
+      const int hp = npass & 1;
       ++npass;
-      hist.cnt[par][tid] = 0u;
-      hist.mass[par][tid] = 0ull;
+      hist.cnt[hp][tid] = 0u;
+      hist.mass[hp][tid] = 0ull;
       if (tid == 0) s_sel = -1;
       __syncthreads();
-      const uint32_t himask = shift + 8 >= 32 ? 0u : ~0u << (shift + 8);
-      auto add = [&](float x) {
-        if (!(x >= lo)) return;
-        const uint32_t kx = fkey(x);
-        if ((kx ^ prefix) & himask) return;
-        const int d = int((kx >> shift) & 255u);
-        atomicAdd(&hist.cnt[par][d], 1u);
+      const uint32_t himask = top >= 32 ? 0u : ~((1u << top) - 1u);
+      const uint32_t dmask = (1u << (top - shift)) - 1u;
+      // warp-uniform: every lane calls with its element (or part = false)
+      auto add = [&](float x, bool part) {
+        int d = -1;
+        if (part && x >= lo) {
+          const uint32_t kx = fkey(x);
+          if (((kx ^ prefix) & himask) == 0u) d = int((kx >> shift) & dmask);
+        }
+        if (!__any_sync(kFullWarp, d >= 0)) return;
+        const unsigned peers = __match_any_sync(kFullWarp, d);
+        if (d < 0) return;
+        const bool leader = lane == __ffs(peers) - 1;
         if (has_p) {
           const float e = exp2f((x - lmax) * c2);
-          atomicAdd(&hist.mass[par][d], __float2ull_rn(e * 1099511627776.0f));
+          const unsigned long long mm = __float2ull_rn(e * 1099511627776.0f);
+          const unsigned hi = __reduce_add_sync(peers, unsigned(mm >> 20));
+          const unsigned lw = __reduce_add_sync(peers, unsigned(mm & 0xFFFFFu));
+          if (leader)
+            atomicAdd(&hist.mass[hp][d], (static_cast<unsigned long long>(hi) << 20) + lw);
         }
+        if (leader) atomicAdd(&hist.cnt[hp][d], unsigned(__popc(peers)));
       };
+      bool ok = true;
       if (from_buffer) {
-        for (int i = tid; i < nbuf; i += kThreads) add(bval[i]);
-      } else {
-        for (int q = tid; q < ch.nvec; q += kThreads) {
-          int i0;
-          const uint32_t cb = ch.bits(q, i0);
-          if (!cb) continue;
-          const uint4 raw = ch.vec(q);
-#pragma unroll
-          for (int e = 0; e < EPV; ++e)
-            if ((cb >> e) & 1u) {
-              const float x = E::get(raw, e);
-              if (x > -INFINITY) add(x);
-            }
+        for (int b0 = warp * 32; b0 < nbuf; b0 += kThreads) {
+          const int i = b0 + lane;
+          add(i < nbuf ? bval[i] : 0.f, i < nbuf);
         }
+      } else {
+        ok = stream(
+            [&](int, bool, const uint4& raw, uint32_t cb, int) {
+              if (!__any_sync(kFullWarp, cb != 0)) return;
+#pragma unroll
+              for (int e = 0; e < EPV; ++e) {
+                const float x = E::get(raw, e);
+                add(x, ((cb >> e) & 1u) && x > -INFINITY);
+              }
+            },
+            []() {});
       }
+      (void)ok;
       __syncthreads();
-      cluster.sync();
-      // merge bin tid over the cluster, then a descending inclusive scan
+      xsync();
+      // bin tid summed over the cluster, then a descending inclusive scan
       unsigned c = 0;
-      unsigned long long m = 0;
+      unsigned long long mass = 0;
       for (int r = 0; r < C; ++r) {
         const Hist* h = cluster.map_shared_rank(&hist, r);
-        c += h->cnt[par][tid];
-        m += h->mass[par][tid];
+        c += h->cnt[hp][tid];
+        mass += h->mass[hp][tid];
       }
       unsigned sc = c;
-      unsigned long long sm = m;
+      unsigned long long smass = mass;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {  // suffix sums within the warp
+      for (int o = 1; o < 32; o <<= 1) {
         const unsigned yc = __shfl_down_sync(kFullWarp, sc, o);
-        const unsigned long long ym = __shfl_down_sync(kFullWarp, sm, o);
+        const unsigned long long ym = __shfl_down_sync(kFullWarp, smass, o);
         if (lane + o < 32) {
           sc += yc;
-          sm += ym;
+          smass += ym;
         }
       }
       if (lane == 0) {
         scan_c[warp] = sc;
-        scan_m[warp] = sm;
+        scan_m[warp] = smass;
       }
       __syncthreads();
       for (int w = warp + 1; w < kWarps; ++w) {
         sc += scan_c[w];
-        sm += scan_m[w];
+        smass += scan_m[w];
       }
       const unsigned cc = above_c + sc;
-      const unsigned long long cm = above_m + sm;
-      const bool ok = cc > 0u && ((has_k && cc >= unsigned(k)) || (has_p && cm >= P));
-      if (ok) atomicMax(&s_sel, tid);
+      const unsigned long long cm = above_m + smass;
+      const bool okb = cc > 0u && ((has_k && cc >= unsigned(k)) || (has_p && cm >= P));
+      if (okb) atomicMax(&s_sel, tid);
       __syncthreads();
       const int sel = s_sel;
       if (sel < 0) return false;
       if (tid == sel) {
         s_above_c = cc - c;
-        s_above_m = cm - m;
+        s_above_m = cm - mass;
       }
       __syncthreads();
       above_c = s_above_c;
       above_m = s_above_m;
       prefix |= uint32_t(sel) << shift;
-      if (shift <= kLastShift) {
+      if (shift == kLow) {
         out_key = prefix;
         return true;
       }
-      shift -= 8;
+      top = shift;
+      shift = max(top - 8, kLow);
     }
   };
 
   float thr = fm;
   bool from_buffer = !any_overflow;
+  const float lo_b = fmaxf(lo_w, fcut);
   if (has_k || has_p) {
     uint32_t kx = 0;
     bool found = false;
     if (from_buffer) {
-      found = descend(true, fcut, kx);
-      if (!found && !(has_m && fm >= fcut)) from_buffer = false;
+      found = descend(true, lo_b, kx);
+      if (!found && !(fm >= lo_b)) from_buffer = false;
     }
-    if (!from_buffer) found = descend(false, fm, kx);
+    if (!from_buffer) found = descend(false, fcut, kx);
     if (found) thr = fmaxf(key_float(kx), fm);
+  } else if (from_buffer && !(fm >= lo_w)) {
+    from_buffer = false;
   }
 
   // ------------------------------------------------------------------- draw
-  if (from_buffer)
-    draw_buffer(thr, nbuf);
-  else
-    draw_chunk(thr);
-  finish_draw();
+  best = -INFINITY;
+  bestv = INT_MAX;
+  if (from_buffer) {
+    for (int i = tid; i < nbuf; i += kThreads) {
+      const float x = bval[i];
+      if (!(x >= thr)) continue;
+      uint4 w;
+      int g = -1;
+      const int v = bidx[i];
+      arg_combine(best, bestv, score_of(__fdiv_rn(x, T), v, w, g), v);
+    }
+  } else {
+    wgrp = -1;
+    stream(
+        [&](int, bool, const uint4& raw, uint32_t cb, int i0) {
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) {
+            const float x = E::get(raw, e);
+            if (!((cb >> e) & 1u) || !(x >= thr) || !(x > -INFINITY)) continue;
+            const float z = __fdiv_rn(x, T);
+            if (z + kGumbelMax < best) continue;
+            const int v = pt.start + i0 + e;
+            arg_combine(best, bestv, score_of(z, v, w4, wgrp), v);
+          }
+        },
+        []() {});
+  }
+  {
+    float wb = best;
+    int wbv = bestv;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float b2 = __shfl_xor_sync(kFullWarp, wb, o);
+      const int bv2 = __shfl_xor_sync(kFullWarp, wbv, o);
+      arg_combine(wb, wbv, b2, bv2);
+    }
+    if (lane == 0) {
+      red_b[warp] = wb;
+      red_bv[warp] = wbv;
+    }
+  }
+  const int late_err = __syncthreads_or(s_err != 0);
+  if (tid == 0) {
+    float wb = -INFINITY;
+    int wbv = INT_MAX;
+    for (int w = 0; w < kWarps; ++w) arg_combine(wb, wbv, red_b[w], red_bv[w]);
+    xchg.best = wb;
+    xchg.best_v = late_err ? -2 : wbv;
+  }
+  xsync();
+  if (rank == 0 && tid == 0) {
+    float wb = -INFINITY;
+    int wbv = INT_MAX;
+    bool bad = false;
+    for (int r = 0; r < C; ++r) {
+      const Xchg* p = cluster.map_shared_rank(&xchg, r);
+      if (p->best_v == -2) bad = true;
+      arg_combine(wb, wbv, p->best, p->best_v);
+    }
+    a.out[row] = bad ? -2 : (wbv == INT_MAX ? -1 : wbv);
+  }
+  leave();
 }
 
 __global__ void philox_kernel(const uint32_t* __restrict__ ctr, const uint32_t* __restrict__ key,
@@ -704,10 +941,6 @@ __global__ void philox_kernel(const uint32_t* __restrict__ ctr, const uint32_t* 
 
 // ------------------------------------------------------------------- host
 
-constexpr int kStaticSmemMargin = 12 * 1024;   // static shared memory of sample_kernel, rounded up
-constexpr int kSmemPerBlockMax = 227 * 1024;
-constexpr int64_t kChunkTargetBytes = 48 * 1024;
-constexpr int64_t kChunkMaxBytes = LP_MAX_SAMPLE_ROW_BYTES / kMaxCluster;
 
 int num_sms() {
   static int n = [] {
@@ -719,61 +952,48 @@ int num_sms() {
   return n;
 }
 
-struct Plan {
-  int C, chunk, cap, mw_off, buf_off, smem;
-  lp_status status;
-};
+// Tokens per CTA when a row is split over S CTAs (a multiple of 32, so a CTA's
+// bitmask words are its own).
+int64_t chunk_for(int64_t V, int S) {
+  int64_t c = (V + S - 1) / S;
+  c = (c + 31) / 32 * 32;
+  return std::max<int64_t>(c, 32);
+}
 
-Plan plan_sample(int64_t B, int64_t V, int eb) {
-  Plan p{};
-  auto chunk_for = [&](int C) {
-    int64_t c = (V + C - 1) / C;
-    c = (c + 31) / 32 * 32;
-    return std::max<int64_t>(c, 32);
-  };
-  int C = 1;
-  while (C < kMaxCluster && chunk_for(C) * eb > kChunkTargetBytes) C *= 2;
-  while (C < kMaxCluster && B * C < 2 * num_sms() && chunk_for(2 * C) >= 4096) C *= 2;
-  const int64_t chunk = chunk_for(C);
-  if (chunk * eb > kChunkMaxBytes) {
-    p.status = LP_ERR_TOO_LARGE;
-    return p;
-  }
-  p.C = C;
-  p.chunk = int(chunk);
-  const int data = int((chunk * eb + 32 + 15) / 16 * 16);
-  const int mw = int((chunk / 32 * 4 + 15) / 16 * 16);
-  int cap = kDefaultCap;
-  while (cap > 256 && data + mw + 8 * cap + kStaticSmemMargin > kSmemPerBlockMax) cap /= 2;
-  p.cap = cap;
-  p.mw_off = data;
-  p.buf_off = data + mw;
-  p.smem = data + mw + 8 * cap;
-  p.status = LP_OK;
-  return p;
+// Split rows over more CTAs while the batch alone gives fewer than about three
+// CTAs per SM (the resident count), keeping at least 4096 tokens per CTA.
+int split_for(int64_t B, int64_t V) {
+  int S = 1;
+  while (S < kMaxSplit && B * S < 3 * int64_t(num_sms()) && chunk_for(V, 2 * S) >= 4096) S *= 2;
+  return S;
 }
 
 template <int DT>
-cudaError_t launch_sample(const SampleArgs& a, const Plan& p, int B, cudaStream_t s) {
+cudaError_t launch_sample(SampleArgs a, int64_t B, int64_t V, cudaStream_t s) {
   static std::mutex mu;
-  static int configured = 0;
+  static bool configured = false;
+  const int S = split_for(B, V);
   {
     std::lock_guard<std::mutex> lock(mu);
-    if (p.smem > configured) {
+    if (!configured) {
       cudaError_t e = cudaFuncSetAttribute(sample_kernel<DT>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem);
+                                           cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
       if (e != cudaSuccess) return e;
-      configured = p.smem;
+      e = cudaFuncSetAttribute(sample_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmem);
+      if (e != cudaSuccess) return e;
+      configured = true;
     }
   }
+  a.chunk = int(chunk_for(V, S));
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(B) * unsigned(p.C));
+  cfg.gridDim = dim3(unsigned(B) * unsigned(S));
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = size_t(p.smem);
+  cfg.dynamicSmemBytes = size_t(kSmem);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = unsigned(p.C);
+  attr[0].val.clusterDim.x = unsigned(S);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -788,11 +1008,10 @@ lp_status run_sample(const void* logits, lp_dtype dt, int64_t B, int64_t vocab,
   if (B == 0) return LP_OK;
   if (logits == nullptr && vocab > 0) return LP_ERR_INVALID_ARGUMENT;
   if (out_ids == nullptr || params == nullptr) return LP_ERR_INVALID_ARGUMENT;
-  if (B > 0x7fffffff / kMaxCluster || vocab > 0x7fffffff || num_indices > 0x7fffffff)
+  if (B * int64_t(kMaxSplit) > 0x7fffffff || vocab > 0x7fffffff - 64 ||
+      num_indices > 0x7fffffff)
     return LP_ERR_TOO_LARGE;
   const int eb = dt == LP_F32 ? 4 : 2;
-  const Plan p = plan_sample(B, vocab, eb);
-  if (p.status != LP_OK) return p.status;
   SampleArgs a{};
   a.logits = static_cast<const char*>(logits);
   a.stride_bytes = logits_stride * eb;
@@ -814,15 +1033,11 @@ lp_status run_sample(const void* logits, lp_dtype dt, int64_t B, int64_t vocab,
   a.seed = params->seed;
   a.offset = params->offset;
   a.out = out_ids;
-  a.chunk = p.chunk;
-  a.cap = p.cap;
-  a.mw_off = p.mw_off;
-  a.buf_off = p.buf_off;
   cudaError_t e;
   switch (dt) {
-    case LP_F32: e = launch_sample<LP_F32>(a, p, int(B), stream); break;
-    case LP_F16: e = launch_sample<LP_F16>(a, p, int(B), stream); break;
-    default: e = launch_sample<LP_BF16>(a, p, int(B), stream); break;
+    case LP_F32: e = launch_sample<LP_F32>(a, B, vocab, stream); break;
+    case LP_F16: e = launch_sample<LP_F16>(a, B, vocab, stream); break;
+    default: e = launch_sample<LP_BF16>(a, B, vocab, stream); break;
   }
   return e == cudaSuccess ? LP_OK : LP_ERR_CUDA;
 }

@@ -48,7 +48,7 @@ typedef enum {
   LP_ERR_INVALID_ARGUMENT = 1,
   LP_ERR_UNSUPPORTED_DTYPE = 2,
   LP_ERR_CUDA = 3,
-  LP_ERR_TOO_LARGE = 4 /* a row longer than the sampler supports (see lp_sample) */
+  LP_ERR_TOO_LARGE = 4 /* a size past the 32-bit index range of the kernels */
 } lp_status;
 
 /*
@@ -122,7 +122,7 @@ lp_status lp_apply_packed_bitmask(void* out, int64_t out_stride, const void* log
  * lp_sample -- Kernel Hub "logits-processor", Ops (sample) and How it works.
  *
  * One token id per row of logits[B, vocab_size] (row stride logits_stride):
- *   candidates C = tokens with a finite-or-+inf logit above -inf;
+ *   candidates C = tokens whose logit is above -inf;
  *   C empty -> -1;
  *   greedy (temperature <= 0 or top_k == 1) -> lowest-index argmax of the logits;
  *   else z = logit / temperature, p = softmax(z) over C, keep every v in C with
@@ -135,10 +135,9 @@ lp_status lp_apply_packed_bitmask(void* out, int64_t out_stride, const void* log
  *   hi32(offset)) and key (lo32(seed), hi32(seed)).
  *   out_ids        device int64 [B]
  *   params         host pointer, see lp_sampling_params
- * Logits are read only.  Rows longer than the sampler's on-chip capacity
- * (LP_MAX_SAMPLE_ROW_BYTES of logits) return LP_ERR_TOO_LARGE.
+ * Logits are read only.  vocab_size up to 2^31 - 65 and B up to 2^27 are
+ * supported; larger sizes return LP_ERR_TOO_LARGE.
  */
-#define LP_MAX_SAMPLE_ROW_BYTES (8 * 200 * 1024)
 
 lp_status lp_sample(const void* logits, lp_dtype dt, int64_t B, int64_t vocab_size,
                     int64_t logits_stride, const lp_sampling_params* params,

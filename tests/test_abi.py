@@ -121,9 +121,11 @@ def test_sample_validation(lib):
     assert lib.lp_sample(FAKE, 0, 2, 10, 10, ctypes.byref(p), None, None) == \
         _lib.LP_ERR_INVALID_ARGUMENT
     assert lib.lp_sample(None, 0, 0, 10, 10, ctypes.byref(p), None, None) == _lib.LP_OK
-    # rows past the sampler's on-chip capacity are refused before any launch
-    huge = 8 * 200 * 1024 // 2 + 64
+    # sizes past the kernels' 32-bit index range are refused before any launch
+    huge = 2**31
     assert lib.lp_sample(FAKE, 1, 2, huge, huge, ctypes.byref(p), out, None) == \
+        _lib.LP_ERR_TOO_LARGE
+    assert lib.lp_sample(FAKE, 1, 2**28, 8, 8, ctypes.byref(p), out, None) == \
         _lib.LP_ERR_TOO_LARGE
 
 

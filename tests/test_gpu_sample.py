@@ -292,21 +292,19 @@ def test_misaligned_rows_and_strides():
             assert np.array_equal(got, want), (dtype, args)
 
 
-def test_longest_supported_row_and_limit():
-    from grammar_constrained_logit_gb300._lib import LPError
-
-    V = 800_000
+def test_long_rows():
+    """Rows of 1.5 M bf16 tokens (split over a cluster of CTAs) and a single row of
+    4 M float32 tokens, all three paths, against the oracle."""
     rng = np.random.default_rng(13)
-    x = (rng.standard_normal((2, V)) * 2).astype(np.float32)
-    st = syn.to_storage(x, "bf16")
-    lg = to_dev(st, "bf16")
-    for args in (dict(temperature=0.0), dict(temperature=1.0, top_k=100),
-                 dict(temperature=1.0, top_p=0.5)):
-        got = ops.sample(lg, seed=9, **args).cpu().numpy()
-        want = oracle.mask_and_sample(st, dtype=oracle.BF16, seed=9, **args)
-        assert np.array_equal(got, want), args
-    with pytest.raises(LPError):
-        ops.sample(torch.zeros(1, 900_000, device="cuda", dtype=torch.bfloat16), 1.0)
+    for B, V, dtype in ((3, 1_500_000, "bf16"), (1, 4_000_000, "f32")):
+        x = (rng.standard_normal((B, V)) * 2).astype(np.float32)
+        st = syn.to_storage(x, dtype)
+        lg = to_dev(st, dtype)
+        for args in (dict(temperature=0.0), dict(temperature=1.0, top_k=100),
+                     dict(temperature=1.0, top_p=0.5), dict(temperature=0.2)):
+            got = ops.sample(lg, seed=9, **args).cpu().numpy()
+            want = oracle.mask_and_sample(st, dtype=DT[dtype], seed=9, **args)
+            assert np.array_equal(got, want), (B, V, args)
 
 
 # ---------------------------------------------------- distribution, determinism
