@@ -536,24 +536,24 @@ def _time_for(fn, seconds: float):
 
 def cpu_baseline(workloads, kinds, seconds: float) -> dict:
     """The oracle, as it stands (single thread), on bounded samples."""
-    out = {"kind": "oracle", "cores": 1}
+    parts = {}
     per = seconds / max(len(workloads), 1)
     for w, kind in zip(workloads, kinds):
         if kind == "apply":
             rows = apply_rows(w)
             per_call, n = _time_for(_oracle_apply_rows(w, rows), per)
             gbs = apply_bytes(w) / per_call / 1e9
-            out["apply"] = {"value": round(gbs, 4), "unit": "GB/s",
-                            "sample": f"{describe(w)}: all {rows} applied rows, {n} repeats"}
+            parts["apply"] = {"value": round(gbs, 4), "unit": "GB/s",
+                              "sample": f"{describe(w)}: all {rows} applied rows, {n} repeats"}
         else:
             nr = min(w.B, 16)
             rows = np.sort(np.random.default_rng(0).choice(w.B, size=nr, replace=False))
             per_call, n = _time_for(_oracle_sample_rows(w, rows), per)
-            out["sample"] = {"value": round(nr / per_call, 3), "unit": "rows/s",
-                             "sample": f"{describe(w)}: {nr} seeded rows, {n} repeats"}
-    head = out.get("apply") or out.get("sample")
-    out["value"], out["unit"], out["sample"] = head["value"], head["unit"], head["sample"]
-    return out
+            parts["sample"] = {"value": round(nr / per_call, 3), "unit": "rows/s",
+                               "sample": f"{describe(w)}: {nr} seeded rows, {n} repeats"}
+    head = parts.get("apply") or parts.get("sample")
+    return {"value": head["value"], "unit": head["unit"], "cores": 1, "kind": "oracle",
+            "sample": head["sample"], "parts": parts}
 
 
 def run_reference(args) -> dict | None:

@@ -125,6 +125,70 @@ struct Elt<LP_F16> {
   }
 };
 
+// ------------------------------------------------------------ vector max
+
+// Max over the elements e of a vector with bit e of `keep` set (-inf if none).
+// 16-bit types take the max of the element pairs with one packed instruction
+// per pair of words; masked elements are first replaced by -inf.
+template <int DT>
+struct VecMax;
+
+template <>
+struct VecMax<LP_F32> {
+  __device__ static __forceinline__ float run(const uint4& v, uint32_t keep) {
+    const float x0 = (keep & 1u) ? __uint_as_float(v.x) : -INFINITY;
+    const float x1 = (keep & 2u) ? __uint_as_float(v.y) : -INFINITY;
+    const float x2 = (keep & 4u) ? __uint_as_float(v.z) : -INFINITY;
+    const float x3 = (keep & 8u) ? __uint_as_float(v.w) : -INFINITY;
+    return fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+  }
+};
+
+template <>
+struct VecMax<LP_BF16> {
+  static constexpr uint32_t kNegInf2 = 0xff80ff80u;
+  __device__ static __forceinline__ uint32_t mx(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+  }
+  __device__ static __forceinline__ float run(const uint4& v, uint32_t keep) {
+    uint32_t w0 = v.x, w1 = v.y, w2 = v.z, w3 = v.w;
+    if (keep != 0xffu) {
+      uint32_t m;
+      m = keep_mask16(keep, 0); w0 = (w0 & m) | (kNegInf2 & ~m);
+      m = keep_mask16(keep, 1); w1 = (w1 & m) | (kNegInf2 & ~m);
+      m = keep_mask16(keep, 2); w2 = (w2 & m) | (kNegInf2 & ~m);
+      m = keep_mask16(keep, 3); w3 = (w3 & m) | (kNegInf2 & ~m);
+    }
+    const uint32_t t = mx(mx(w0, w1), mx(w2, w3));
+    return fmaxf(__uint_as_float(t << 16), __uint_as_float(t & 0xffff0000u));
+  }
+};
+
+template <>
+struct VecMax<LP_F16> {
+  static constexpr uint32_t kNegInf2 = 0xfc00fc00u;
+  __device__ static __forceinline__ uint32_t mx(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+  }
+  __device__ static __forceinline__ float run(const uint4& v, uint32_t keep) {
+    uint32_t w0 = v.x, w1 = v.y, w2 = v.z, w3 = v.w;
+    if (keep != 0xffu) {
+      uint32_t m;
+      m = keep_mask16(keep, 0); w0 = (w0 & m) | (kNegInf2 & ~m);
+      m = keep_mask16(keep, 1); w1 = (w1 & m) | (kNegInf2 & ~m);
+      m = keep_mask16(keep, 2); w2 = (w2 & m) | (kNegInf2 & ~m);
+      m = keep_mask16(keep, 3); w3 = (w3 & m) | (kNegInf2 & ~m);
+    }
+    const uint32_t t = mx(mx(w0, w1), mx(w2, w3));
+    return fmaxf(Elt<LP_F16>::half_bits_to_float(t & 0xffffu),
+                 Elt<LP_F16>::half_bits_to_float(t >> 16));
+  }
+};
+
 // ------------------------------------------------------------- bitmask bits
 
 // Bits [0, n) of the result are the bitmask bits of tokens j .. j+n-1 of one

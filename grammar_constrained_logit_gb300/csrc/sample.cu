@@ -3,14 +3,15 @@
 // unsatisfiable rows as in TensorRT-Edge-LLM "Guided Decoder").
 //
 // GB300 design: one streaming pass over HBM through the Tensor Memory
-// Accelerator.  A row is split over a thread-block cluster of S CTAs (S = 1 for
-// big batches).  Each CTA streams its part of the row through a ring of four
-// 8 KB shared-memory stages: one thread keeps bulk copies (cp.async.bulk, with
-// the stage's bitmask words) in flight on mbarriers, the 256 threads consume
-// each landed stage from shared memory.  Three CTAs share an SM, so many rows'
-// reduction chains are in flight at once.  The CTAs of a row combine partial
-// results through distributed shared memory (DSMEM) behind cluster barriers;
-// nothing is written to global memory but the ids.
+// Accelerator, in a persistent grid.  A row is split over a thread-block cluster
+// of S CTAs; the resident clusters take the rows round-robin.  Each CTA streams
+// its parts of its rows through a ring of four 8 KB shared-memory stages: one
+// thread keeps bulk copies (cp.async.bulk, with the stage's bitmask words) in
+// flight on mbarriers, running up to one row ahead, so the next row's loads
+// overlap this row's reductions; the 256 threads consume each landed stage from
+// shared memory.  The CTAs of a row combine partial results through distributed
+// shared memory (DSMEM) behind cluster barriers; nothing is written to global
+// memory but the ids.
 //
 // Per row, in the stream:
 //   * candidate max, the vector holding it (its lowest index is found after the
@@ -59,6 +60,7 @@ constexpr int kRing = 4;                 // stages in flight per CTA
 constexpr int kPieceBytes = 8192;        // bytes of logits per stage
 constexpr int kPieceWords = kPieceBytes / 2 / 32 + 2;  // bitmask words a stage can need
 constexpr int kMaskSlot = (16 + 4 * kPieceWords + 15) / 16 * 16;
+constexpr int kPerPiece = kPieceBytes / 16 / 256;  // vectors of a piece per thread
 constexpr int kKBins = 128;              // log-spaced bins of (row max - thread max)
 constexpr int kKBase = (127 - 6) << 3;   // code of 2^-6 (8 exponent + 3 fraction bits)
 constexpr int kMaxSplit = 16;
@@ -89,6 +91,7 @@ struct SampleArgs {
   uint64_t seed, offset;
   int64_t* out;
   int chunk;  // tokens per CTA (a multiple of 32)
+  int ncl;    // clusters in the grid; cluster c owns rows c, c + ncl, ...
 };
 
 struct Xchg {  // per-CTA values read by the other CTAs of the cluster
@@ -296,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleArgs a)
   cg::cluster_group cluster = cg::this_cluster();
   const int C = int(cluster.num_blocks());
   const int rank = int(cluster.block_rank());
-  const int row = int(blockIdx.x) / C;
+  const int cid = int(blockIdx.x) / C;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   auto xsync = [&]() {
     if (C > 1)
@@ -311,618 +314,645 @@ __global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleArgs a)
   float* const bval = reinterpret_cast<float*>(mring + kRing * kMaskSlot);
   int* const bidx = reinterpret_cast<int*>(bval + kCap);
 
-  __shared__ Xchg xchg;
-  __shared__ float tmaxs[kThreads];
-  __shared__ Hist hist;
+  __shared__ Xchg xchg[2];              // by row parity: read by peers without a trailing barrier
+  __shared__ float tmaxs[2][kThreads];  // per-thread maxima, by row parity
+  __shared__ Hist hist;                 // by radix-pass parity
   __shared__ float red_f[kWarps], red_s[kWarps], red_b[kWarps];
   __shared__ int red_i[kWarps], red_n[kWarps], red_bv[kWarps];
   __shared__ unsigned scan_c[kWarps];
   __shared__ unsigned long long scan_m[kWarps];
   __shared__ unsigned kmerge[kKBins];
   __shared__ int s_count, s_sel, s_err, s_i[4];
-  __shared__ float s_f[2];
+  __shared__ float s_f[3];
   __shared__ unsigned s_runkey, s_above_c;
   __shared__ unsigned long long s_above_m;
+  __shared__ int s_masked[2];  // masked flag of the row of each parity
   __shared__ __align__(8) uint64_t full[kRing];
+  __shared__ int4 pmeta[kRing];  // per slot: vectors [x, y), staged mask words [z, w)
+  __shared__ int pwhole[kRing];  // per slot: every vector of the piece is a whole vector
 
-  // ------------------------------------------------------------ row set-up
-  const float T = a.temp ? a.temp[row] : a.temp_s;
-  int k = a.topk ? a.topk[row] : a.topk_s;
-  const float tp = a.topp ? a.topp[row] : a.topp_s;
-  const float mp = a.minp ? a.minp[row] : a.minp_s;
-  const bool greedy = !(T > 0.f) || k == 1;
-  const bool has_p = !greedy && tp < 1.f;
-  const bool has_m = !greedy && mp > 0.f;
-  const bool has_k0 = !greedy && k > 0;
-  const bool unfiltered = !greedy && !has_p && !has_m && !has_k0;
-  const bool compact = !greedy && !unfiltered;
-  const float c2 = greedy ? 0.f : kLog2e / T;
-  const float tl = has_m ? T * logf(mp) : 0.f;  // min-p bound below the maximum: max + tl
-  float delta = INFINITY;                       // the compaction window below the running max
-  if (has_m) delta = fminf(delta, -tl);
-  if (has_p) delta = fminf(delta, T * (2.f + 2.5f * logf(1.f / fmaxf(1.f - tp, 1e-6f))));
-  if (has_k0) delta = fminf(delta, kWindowK);
-  if (!(delta > 0.f)) delta = 0.f;
-
-  bool masked = false;
-  if (a.bitmask) {
-    if (a.indices == nullptr) {
-      masked = true;
-    } else {
-      int found = 0;
-      for (int i = tid; i < a.n_indices; i += kThreads) found |= (a.indices[i] == row);
-      masked = __syncthreads_or(found) != 0 && row < a.bm_rows;
-    }
-  }
-  Pt pt;
-  pt.init(a, row, rank, masked);
   if (tid == 0) {
-    s_count = 0;
     s_err = 0;
-    s_runkey = fkey(-INFINITY);
     for (int r = 0; r < kRing; ++r) mbar_init(&full[r], 1);
     mbar_init_fence();
   }
-  if (tid < kKBins) kmerge[tid] = 0u;
   __syncthreads();
 
-  // ------------------------------------------------------------ the ring
-  uint32_t ring_next = 0;  // pieces issued (all passes); slot = n % kRing
-  uint32_t ring_done = 0;  // pieces consumed
-  uint32_t lost = 0;       // bit s: this thread's wait on slot s timed out (parity in bit s + 8)
-  // Thread 0 arms slot (n % kRing) and starts the copies of piece j.
-  auto issue_piece = [&](int j) {
-    const int slot = int(ring_next % kRing);
-    ++ring_next;
-    if (tid != 0) return;
+  const uint2 key = make_uint2(uint32_t(a.seed), uint32_t(a.seed >> 32));
+  auto row_of = [&](int it) { return cid + it * a.ncl; };
+  auto masked_of = [&](int row) -> bool {  // block-uniform
+    if (!a.bitmask) return false;
+    if (a.indices == nullptr) return true;
+    int found = 0;
+    for (int i = tid; i < a.n_indices; i += kThreads) found |= (a.indices[i] == row);
+    return __syncthreads_or(found) != 0 && row < a.bm_rows;
+  };
+
+  // ---------------------------------------------------------------- the ring
+  // Pieces of this CTA's rows are copied in row order into slot (n % kRing) of
+  // the n-th piece; thread 0 keeps up to kRing of them in flight, at most one
+  // row ahead of the row being consumed, so the next row's loads overlap this
+  // row's reductions.
+  uint32_t issued = 0, consumed = 0, lost = 0;
+  int p_iter = 0, p_piece = 0;  // producer position (thread 0)
+  auto issue = [&](const Pt& g, int j) {
+    const int slot = int(issued % kRing);
+    ++issued;
     int q0, q1;
-    pt.piece_vecs(j, q0, q1);
-    const int v0 = max(q0, pt.qf0), v1 = min(q1, pt.qf1);
+    g.piece_vecs(j, q0, q1);
+    const int v0 = max(q0, g.qf0), v1 = min(q1, g.qf1);
     const uint32_t vbytes = v1 > v0 ? uint32_t(16 * (v1 - v0)) : 0u;
     uint32_t mbytes = 0;
     int w0 = 0, w1 = 0, m_lo = 0, m_hi = 0, mmis = 0;
-    if (pt.masked) {
-      pt.piece_words(j, w0, w1);
-      pt.mask_interior(w0, w1, m_lo, m_hi, mmis);
+    if (g.masked) {
+      g.piece_words(j, w0, w1);
+      g.mask_interior(w0, w1, m_lo, m_hi, mmis);
       mbytes = uint32_t(4 * (m_hi - m_lo));
     }
-    if (s_err) {  // a copy went missing earlier: start no more; the row reports -2
+    pmeta[slot] = make_int4(q0, q1, m_lo, m_hi);  // published by the arrive below
+    pwhole[slot] = q0 >= g.qf0 && q1 <= g.qf1;
+    if (s_err) {  // a copy went missing earlier: start no more (rows report -2)
       mbar_expect_tx(&full[slot], 0);
       return;
     }
     mbar_expect_tx(&full[slot], vbytes + mbytes);
     if (vbytes)
-      bulk_load(ring + slot * kPieceBytes + 16 * (v0 - q0), pt.g0 + 16 * v0, vbytes, &full[slot]);
-    if (mbytes)
-      bulk_load(mring + slot * kMaskSlot, pt.gmask + m_lo, mbytes, &full[slot]);
+      bulk_load(ring + slot * kPieceBytes + 16 * (v0 - q0), g.g0 + 16 * v0, vbytes, &full[slot]);
+    if (mbytes) bulk_load(mring + slot * kMaskSlot, g.gmask + m_lo, mbytes, &full[slot]);
   };
-  // Streams the part once: f(q, valid, raw, cb, i0) for every vector q, in
-  // warp-uniform iterations (valid false on padding lanes); after each
-  // iteration, g() (also warp-uniform).  Returns false if a stage never landed.
-  auto stream = [&](auto&& f, auto&& g) {
-    const int np = pt.npieces;
-    for (int j = 0; j < min(np, kRing); ++j) issue_piece(j);
-    bool ok = true;
-    for (int j = 0; j < np; ++j) {
-      const int slot = int(ring_done % kRing);
-      const uint32_t parity = (ring_done / kRing) & 1u;
-      ++ring_done;
+  auto top_up = [&](int cur) {  // thread 0 only
+    while (issued - consumed < uint32_t(kRing)) {
+      const int prow = row_of(p_iter);
+      if (prow >= a.B || p_iter > cur + 1) break;
+      Pt g;
+      g.init(a, prow, rank, s_masked[p_iter & 1] != 0);
+      if (p_piece < g.npieces) {
+        issue(g, p_piece);
+        ++p_piece;
+      } else {
+        ++p_iter;
+        p_piece = 0;
+      }
+    }
+  };
+
+  if (row_of(0) < a.B) {
+    const bool m0 = masked_of(row_of(0));
+    if (tid == 0) s_masked[0] = m0;
+  }
+  int npass = 0;  // radix passes so far: histogram parity
+
+  for (int it = 0; row_of(it) < a.B; ++it) {
+    const int row = row_of(it);
+    const int par = it & 1;
+    __syncthreads();  // the previous row is done in this CTA
+    if (row_of(it + 1) < a.B) {
+      const bool mn = masked_of(row_of(it + 1));
+      if (tid == 0) s_masked[par ^ 1] = mn;
+    }
+    if (tid == 0) {
+      s_count = 0;
+      s_runkey = fkey(-INFINITY);
+    }
+    if (tid < kKBins) kmerge[tid] = 0u;
+    __syncthreads();
+    if (tid == 0) top_up(it);
+
+    Pt pt;
+    pt.init(a, row, rank, s_masked[par] != 0);
+    const float T = a.temp ? a.temp[row] : a.temp_s;
+    int k = a.topk ? a.topk[row] : a.topk_s;
+    const float tp = a.topp ? a.topp[row] : a.topp_s;
+    const float mp = a.minp ? a.minp[row] : a.minp_s;
+    const bool greedy = !(T > 0.f) || k == 1;
+    const bool has_p = !greedy && tp < 1.f;
+    const bool has_m = !greedy && mp > 0.f;
+    const bool has_k0 = !greedy && k > 0;
+    const bool unfiltered = !greedy && !has_p && !has_m && !has_k0;
+    const bool compact = !greedy && !unfiltered;
+    const float c2 = greedy ? 0.f : kLog2e / T;
+    const float tl = has_m ? T * logf(mp) : 0.f;  // min-p bound below the maximum: max + tl
+    float delta = INFINITY;                       // compaction window below the running max
+    if (has_m) delta = fminf(delta, -tl);
+    if (has_p) delta = fminf(delta, T * (2.f + 2.5f * logf(1.f / fmaxf(1.f - tp, 1e-6f))));
+    if (has_k0) delta = fminf(delta, kWindowK);
+    if (!(delta > 0.f)) delta = 0.f;
+
+    // Gumbel score of candidate (z = x / T, token v); w4/wgrp cache v's Philox block
+    auto score_of = [&](float z, int v, uint4& w4, int& wgrp) {
+      const int grp = v >> 2;
+      if (grp != wgrp) {
+        w4 = philox4x32_10(make_uint4(uint32_t(grp), uint32_t(row), uint32_t(a.offset),
+                                      uint32_t(a.offset >> 32)),
+                           key);
+        wgrp = grp;
+      }
+      const uint32_t word = (v & 3) == 0 ? w4.x : (v & 3) == 1 ? w4.y : (v & 3) == 2 ? w4.z : w4.w;
+      return z + gumbel_from_word(word);
+    };
+
+    // ------------------------------------------------- stream the row part
+    float m = -INFINITY, sm = 0.f;  // running max and softmax sum relative to it
+    int mq = -1, cnt = 0;           // vector of the running max; candidate bits seen
+    float best = -INFINITY;         // unfiltered rows: running best score
+    int bestv = INT_MAX;
+    uint4 w4 = make_uint4(0, 0, 0, 0);
+    int wgrp = -1;
+    bool stream_ok = true;
+    for (int j = 0; j < pt.npieces; ++j) {
+      const int slot = int(consumed % kRing);
+      const uint32_t parity = (consumed / kRing) & 1u;
+      ++consumed;
       if (!mbar_wait(&full[slot], parity)) {
-        ok = false;
+        stream_ok = false;
         s_err = 1;
         lost |= (1u << slot) | (parity << (slot + 8));
       }
-      int q0, q1, w0 = 0, w1 = 0, m_lo = 0, m_hi = 0, mmis = 0;
-      pt.piece_vecs(j, q0, q1);
-      if (pt.masked) {
-        pt.piece_words(j, w0, w1);
-        pt.mask_interior(w0, w1, m_lo, m_hi, mmis);
-      }
+      const int4 pm = pmeta[slot];
+      const bool whole = pwhole[slot] != 0;
       const unsigned char* data = ring + slot * kPieceBytes;
       const uint32_t* mw = reinterpret_cast<const uint32_t*>(mring + slot * kMaskSlot);
-      for (int base = q0; base < q1; base += kThreads) {
-        const int q = base + tid;
-        const bool valid = q < q1;
-        int i0 = 0;
-        uint32_t cb = 0;
-        uint4 raw = make_uint4(0, 0, 0, 0);
-        if (valid) {
-          cb = pt.bits(q, i0, mw, m_lo, m_hi);
-          if (cb)
-            raw = (q >= pt.qf0 && q < pt.qf1)
-                      ? *reinterpret_cast<const uint4*>(data + 16 * (q - q0))
-                      : pt.gvec(q);
+      // vector q of this piece and its candidate bits
+      auto load = [&](int q, uint4& raw, uint32_t& cb) {
+        const bool staged = whole || (q >= pt.qf0 && q < pt.qf1);
+        raw = staged ? *reinterpret_cast<const uint4*>(data + 16 * (q - pm.x)) : pt.gvec(q);
+        int i0;
+        cb = (whole && !pt.masked) ? Pt::ALL : pt.bits(q, i0, mw, pm.z, pm.w);
+      };
+      float vms[kPerPiece];
+#pragma unroll
+      for (int r = 0; r < kPerPiece; ++r) {
+        const int q = pm.x + r * kThreads + tid;
+        vms[r] = -INFINITY;
+        if (q >= pm.y) continue;
+        uint4 raw;
+        uint32_t cb;
+        load(q, raw, cb);
+        if (!cb) continue;
+        const float vm = VecMax<DT>::run(raw, cb);
+        vms[r] = vm;
+        cnt += __popc(cb);
+        if (vm > m) {
+          if (has_p && m > -INFINITY) sm *= exp2f((m - vm) * c2);
+          m = vm;
+          mq = q;
         }
-        f(q, valid, raw, cb, i0);
-        g();
+        if (has_p) {
+          const float off = m * c2;
+#pragma unroll
+          for (int e = 0; e < EPV; ++e)
+            if ((cb >> e) & 1u) sm += exp2f(fmaf(E::get(raw, e), c2, -off));
+        }
+        if (unfiltered) {
+          const int i0 = (16 * q - pt.mis) / Pt::EB;
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) {
+            const float x = E::get(raw, e);
+            if (!((cb >> e) & 1u) || !(x > -INFINITY)) continue;
+            const float z = __fdiv_rn(x, T);
+            if (z + kGumbelMax < best) continue;  // cannot win
+            const int v = pt.start + i0 + e;
+            arg_combine(best, bestv, score_of(z, v, w4, wgrp), v);
+          }
+        }
+      }
+      if (compact) {  // warp-uniform: append the piece's candidates within the window
+        float wm = m;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(kFullWarp, wm, o));
+        if (lane == 0 && wm > -INFINITY) atomicMax(&s_runkey, fkey(wm));
+        const float rm = fmaxf(wm, key_float(*(volatile unsigned*)&s_runkey));
+        const float cut = __fsub_rd(rm, delta);
+#pragma unroll
+        for (int r = 0; r < kPerPiece; ++r) {
+          // a lane without a vector has vms = -inf, which must not pass a cut of -inf
+          const bool live = vms[r] > -INFINITY && vms[r] >= cut;
+          if (!__any_sync(kFullWarp, live)) continue;
+          const int q = pm.x + r * kThreads + tid;
+          uint32_t pass = 0;
+          uint4 raw = make_uint4(0, 0, 0, 0);
+          if (live) {
+            uint32_t cb;
+            load(q, raw, cb);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) {
+              const float x = E::get(raw, e);
+              if (((cb >> e) & 1u) && x >= cut && x > -INFINITY) pass |= 1u << e;
+            }
+          }
+          const int n = __popc(pass);
+          int incl = n;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(kFullWarp, incl, o);
+            if (lane >= o) incl += y;
+          }
+          int pos = 0;
+          if (lane == 31) pos = atomicAdd(&s_count, incl);
+          pos = __shfl_sync(kFullWarp, pos, 31) + incl - n;
+          const int i0 = (16 * q - pt.mis) / Pt::EB;
+          while (pass) {
+            const int e = __ffs(pass) - 1;
+            pass &= pass - 1;
+            if (pos < kCap) {
+              bval[pos] = E::get(raw, e);
+              bidx[pos] = pt.start + i0 + e;
+            }
+            ++pos;
+          }
+        }
       }
       __syncthreads();  // every thread is done with the slot
-      if (j + kRing < np) issue_piece(j + kRing);
+      if (tid == 0) top_up(it);
     }
-    return ok;
-  };
 
-  const uint2 key = make_uint2(uint32_t(a.seed), uint32_t(a.seed >> 32));
-  // Gumbel score of candidate (z = x / T, token v); w4/wgrp cache v's Philox block
-  auto score_of = [&](float z, int v, uint4& w4, int& wgrp) {
-    const int grp = v >> 2;
-    if (grp != wgrp) {
-      w4 = philox4x32_10(make_uint4(uint32_t(grp), uint32_t(row), uint32_t(a.offset),
-                                    uint32_t(a.offset >> 32)),
-                         key);
-      wgrp = grp;
-    }
-    const uint32_t word = (v & 3) == 0 ? w4.x : (v & 3) == 1 ? w4.y : (v & 3) == 2 ? w4.z : w4.w;
-    return z + gumbel_from_word(word);
-  };
-
-  // -------------------------------------------------------------- stream
-  float m = -INFINITY, sm = 0.f;  // running max and softmax sum relative to it
-  int mq = -1, cnt = 0;           // vector of the running max; candidate bits seen
-  float best = -INFINITY;         // unfiltered rows: running best score
-  int bestv = INT_MAX;
-  uint4 w4 = make_uint4(0, 0, 0, 0);
-  int wgrp = -1;
-  // this iteration's vector (kept for the compaction step that follows it)
-  uint4 it_raw = make_uint4(0, 0, 0, 0);
-  uint32_t it_cb = 0;
-  int it_i0 = 0;
-  float it_vm = -INFINITY;
-  auto on_vec = [&](int q, bool valid, const uint4& raw, uint32_t cb, int i0) {
-    it_raw = raw;
-    it_cb = cb;
-    it_i0 = i0;
-    it_vm = -INFINITY;
-    if (!cb) return;
-    cnt += __popc(cb);
-    float xs[EPV];
+    // -------------------------------------------------------- row summaries
+    tmaxs[par][tid] = m;
+    int targ = INT_MAX;
+    if (mq >= 0) {  // lowest index of the thread's maximum, in the first vector holding it
+      int i0;
+      const uint32_t cb = pt.bits(mq, i0, nullptr, 0, 0);
+      const uint4 raw = pt.gvec(mq);
 #pragma unroll
-    for (int e = 0; e < EPV; ++e) {
-      xs[e] = ((cb >> e) & 1u) ? E::get(raw, e) : -INFINITY;
-      it_vm = fmaxf(it_vm, xs[e]);
+      for (int e = EPV - 1; e >= 0; --e)
+        if (((cb >> e) & 1u) && E::get(raw, e) == m) targ = pt.start + i0 + e;
     }
-    if (it_vm > m) {
-      if (has_p && m > -INFINITY) sm *= exp2f((m - it_vm) * c2);
-      m = it_vm;
-      mq = q;
-    }
-    if (has_p) {
-      const float off = m * c2;
+    {
+      float wm = m, ws = sm, wb = best;
+      int wv = targ, wn = cnt, wbv = bestv;
 #pragma unroll
-      for (int e = 0; e < EPV; ++e) sm += exp2f(fmaf(xs[e], c2, -off));
-    }
-    if (unfiltered) {
-#pragma unroll
-      for (int e = 0; e < EPV; ++e) {
-        if (!(xs[e] > -INFINITY)) continue;
-        const float z = __fdiv_rn(xs[e], T);
-        if (z + kGumbelMax < best) continue;  // cannot win
-        const int v = pt.start + i0 + e;
-        arg_combine(best, bestv, score_of(z, v, w4, wgrp), v);
+      for (int o = 16; o; o >>= 1) {
+        const float m2 = __shfl_xor_sync(kFullWarp, wm, o);
+        const float s2 = __shfl_xor_sync(kFullWarp, ws, o);
+        const int v2 = __shfl_xor_sync(kFullWarp, wv, o);
+        wn += __shfl_xor_sync(kFullWarp, wn, o);
+        row_combine(wm, wv, ws, m2, v2, s2, c2, has_p);
+        if (unfiltered) {
+          const float b2 = __shfl_xor_sync(kFullWarp, wb, o);
+          const int bv2 = __shfl_xor_sync(kFullWarp, wbv, o);
+          arg_combine(wb, wbv, b2, bv2);
+        }
+      }
+      if (lane == 0) {
+        red_f[warp] = wm;
+        red_s[warp] = ws;
+        red_i[warp] = wv;
+        red_n[warp] = wn;
+        red_b[warp] = wb;
+        red_bv[warp] = wbv;
       }
     }
-  };
-  // filtered rows: append this iteration's candidates within the window
-  auto on_iter = [&]() {
-    if (!compact) return;
-    float wm = m;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(kFullWarp, wm, o));
-    if (lane == 0 && wm > -INFINITY) atomicMax(&s_runkey, fkey(wm));
-    const float rm = fmaxf(wm, key_float(*(volatile unsigned*)&s_runkey));
-    const float cut = __fsub_rd(rm, delta);
-    if (!__any_sync(kFullWarp, it_vm >= cut)) return;
-    uint32_t pass = 0;
-    if (it_vm >= cut) {
-#pragma unroll
-      for (int e = 0; e < EPV; ++e) {
-        const float x = E::get(it_raw, e);
-        if (((it_cb >> e) & 1u) && x >= cut && x > -INFINITY) pass |= 1u << e;
+    const int cta_err = __syncthreads_or(!stream_ok || s_err != 0);
+    if (warp == 0) {
+      float wm = -INFINITY, ws = 0.f, wb = -INFINITY;
+      int wv = INT_MAX, wn = 0, wbv = INT_MAX;
+      if (lane < kWarps) {
+        wm = red_f[lane];
+        ws = red_s[lane];
+        wv = red_i[lane];
+        wn = red_n[lane];
+        wb = red_b[lane];
+        wbv = red_bv[lane];
       }
-    }
-    const int n = __popc(pass);
-    int incl = n;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(kFullWarp, incl, o);
-      if (lane >= o) incl += y;
-    }
-    int pos = 0;
-    if (lane == 31) pos = atomicAdd(&s_count, incl);
-    pos = __shfl_sync(kFullWarp, pos, 31) + incl - n;
-    while (pass) {
-      const int e = __ffs(pass) - 1;
-      pass &= pass - 1;
-      if (pos < kCap) {
-        bval[pos] = E::get(it_raw, e);
-        bidx[pos] = pt.start + it_i0 + e;
-      }
-      ++pos;
-    }
-  };
-  const bool stream_ok = stream(on_vec, on_iter);
-
-  // ------------------------------------------------------ row summaries
-  tmaxs[tid] = m;
-  int targ = INT_MAX;
-  if (mq >= 0) {  // lowest index of the thread's maximum, in the first vector holding it
-    int i0;
-    const uint32_t cb = pt.bits(mq, i0, nullptr, 0, 0);
-    const uint4 raw = pt.gvec(mq);
-#pragma unroll
-    for (int e = EPV - 1; e >= 0; --e)
-      if (((cb >> e) & 1u) && E::get(raw, e) == m) targ = pt.start + i0 + e;
-  }
-  {
-    float wm = m, ws = sm, wb = best;
-    int wv = targ, wn = cnt, wbv = bestv;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float m2 = __shfl_xor_sync(kFullWarp, wm, o);
-      const float s2 = __shfl_xor_sync(kFullWarp, ws, o);
-      const int v2 = __shfl_xor_sync(kFullWarp, wv, o);
-      wn += __shfl_xor_sync(kFullWarp, wn, o);
-      row_combine(wm, wv, ws, m2, v2, s2, c2, has_p);
-      if (unfiltered) {
+      for (int o = 4; o; o >>= 1) {
+        const float m2 = __shfl_xor_sync(kFullWarp, wm, o);
+        const float s2 = __shfl_xor_sync(kFullWarp, ws, o);
+        const int v2 = __shfl_xor_sync(kFullWarp, wv, o);
+        wn += __shfl_xor_sync(kFullWarp, wn, o);
+        row_combine(wm, wv, ws, m2, v2, s2, c2, has_p);
         const float b2 = __shfl_xor_sync(kFullWarp, wb, o);
         const int bv2 = __shfl_xor_sync(kFullWarp, wbv, o);
         arg_combine(wb, wbv, b2, bv2);
       }
+      if (lane == 0) {
+        Xchg& x = xchg[par];
+        x.max = wm;
+        x.arg = wv;
+        x.sum = ws;
+        x.ncand = wn;
+        x.best = wb;
+        x.best_v = wbv;
+        x.overflow = s_count > kCap;
+        x.err = cta_err;
+      }
     }
-    if (lane == 0) {
-      red_f[warp] = wm;
-      red_s[warp] = ws;
-      red_i[warp] = wv;
-      red_n[warp] = wn;
-      red_b[warp] = wb;
-      red_bv[warp] = wbv;
-    }
-  }
-  const int cta_err = __syncthreads_or(!stream_ok);
-  if (warp == 0) {
-    float wm = -INFINITY, ws = 0.f, wb = -INFINITY;
-    int wv = INT_MAX, wn = 0, wbv = INT_MAX;
-    if (lane < kWarps) {
-      wm = red_f[lane];
-      ws = red_s[lane];
-      wv = red_i[lane];
-      wn = red_n[lane];
-      wb = red_b[lane];
-      wbv = red_bv[lane];
-    }
-#pragma unroll
-    for (int o = 4; o; o >>= 1) {
-      const float m2 = __shfl_xor_sync(kFullWarp, wm, o);
-      const float s2 = __shfl_xor_sync(kFullWarp, ws, o);
-      const int v2 = __shfl_xor_sync(kFullWarp, wv, o);
-      wn += __shfl_xor_sync(kFullWarp, wn, o);
-      row_combine(wm, wv, ws, m2, v2, s2, c2, has_p);
-      const float b2 = __shfl_xor_sync(kFullWarp, wb, o);
-      const int bv2 = __shfl_xor_sync(kFullWarp, wbv, o);
-      arg_combine(wb, wbv, b2, bv2);
-    }
-    if (lane == 0) {
-      xchg.max = wm;
-      xchg.arg = wv;
-      xchg.sum = ws;
-      xchg.ncand = wn;
-      xchg.best = wb;
-      xchg.best_v = wbv;
-      xchg.overflow = s_count > kCap;
-      xchg.err = cta_err;
-    }
-  }
-  xsync();  // #1: every CTA's summary is visible to its cluster
-  if (warp == 0) {
-    float wm = -INFINITY, ws = 0.f, wb = -INFINITY;
-    int wv = INT_MAX, wn = 0, wbv = INT_MAX, ov = 0, er = 0;
-    if (lane < C) {
-      const Xchg* p = cluster.map_shared_rank(&xchg, lane);
-      wm = p->max;
-      wv = p->arg;
-      ws = p->sum;
-      wn = p->ncand;
-      wb = p->best;
-      wbv = p->best_v;
-      ov = p->overflow;
-      er = p->err;
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float m2 = __shfl_xor_sync(kFullWarp, wm, o);
-      const float s2 = __shfl_xor_sync(kFullWarp, ws, o);
-      const int v2 = __shfl_xor_sync(kFullWarp, wv, o);
-      wn += __shfl_xor_sync(kFullWarp, wn, o);
-      row_combine(wm, wv, ws, m2, v2, s2, c2, has_p);
-      const float b2 = __shfl_xor_sync(kFullWarp, wb, o);
-      const int bv2 = __shfl_xor_sync(kFullWarp, wbv, o);
-      arg_combine(wb, wbv, b2, bv2);
-    }
-    ov = __any_sync(kFullWarp, ov != 0);
-    er = __any_sync(kFullWarp, er != 0);
-    if (lane == 0) {
-      s_f[0] = wm;
-      s_f[1] = ws;
-      s_i[0] = wv;
-      s_i[1] = wn;
-      s_i[2] = wbv;
-      s_i[3] = ov | (er << 1);
-    }
-  }
-  __syncthreads();
-  const float lmax = s_f[0];
-  const float S = s_f[1];
-  const int larg = s_i[0];
-  const int ncand_ub = s_i[1];  // candidates counted by their bits (-inf included)
-  const bool row_err = (s_i[3] >> 1) != 0;
-
-  // a CTA leaves only once its ring is idle and its peers are done reading it:
-  // a stage whose wait timed out gets one more bounded wait for its copies
-  auto leave = [&]() {
-    for (int sl = 0; sl < kRing; ++sl)
-      if ((lost >> sl) & 1u) (void)mbar_wait(&full[sl], (lost >> (sl + 8)) & 1u);
-    if (C > 1) cluster.sync();
-  };
-  if (row_err || lmax == -INFINITY || greedy || unfiltered) {
-    if (rank == 0 && tid == 0)
-      a.out[row] = row_err ? -2
-                   : lmax == -INFINITY ? -1
-                   : greedy ? larg
-                            : (s_i[2] == INT_MAX ? -1 : s_i[2]);
-    leave();
-    return;
-  }
-  const bool any_overflow = (s_i[3] & 1) != 0;
-  const int nbuf = min(s_count, kCap);
-
-  // --------------------------------------------------------- filter bounds
-  if (k > 0 && k >= ncand_ub) k = 0;  // keeps every candidate
-  const bool has_k = k > 0;
-  const float fm = has_m ? fminf(__fadd_ru(lmax, tl), lmax) : -INFINITY;
-  // top-k: the k-th largest per-thread maximum of the cluster bounds t_k from below
-  int jk = -1;
-  if (has_k && k <= C * kThreads) {
-    for (int r = 0; r < C; ++r) {
-      const float v = cluster.map_shared_rank(&tmaxs[0], r)[tid];
-      if (v > -INFINITY) atomicAdd(&kmerge[kbin(lmax - v)], 1u);
-    }
-    __syncthreads();
+    xsync();  // #1: every CTA's summary is visible to its cluster
     if (warp == 0) {
-      const unsigned c0 = kmerge[4 * lane], c1 = kmerge[4 * lane + 1];
-      const unsigned cc2 = kmerge[4 * lane + 2], c3 = kmerge[4 * lane + 3];
-      unsigned incl = c0 + c1 + cc2 + c3;
+      float wm = -INFINITY, ws = 0.f, wb = -INFINITY;
+      int wv = INT_MAX, wn = 0, wbv = INT_MAX, ov = 0, er = 0;
+      if (lane < C) {
+        const Xchg* p = cluster.map_shared_rank(&xchg[par], lane);
+        wm = p->max;
+        wv = p->arg;
+        ws = p->sum;
+        wn = p->ncand;
+        wb = p->best;
+        wbv = p->best_v;
+        ov = p->overflow;
+        er = p->err;
+      }
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned y = __shfl_up_sync(kFullWarp, incl, o);
-        if (lane >= o) incl += y;
+      for (int o = 16; o; o >>= 1) {
+        const float m2 = __shfl_xor_sync(kFullWarp, wm, o);
+        const float s2 = __shfl_xor_sync(kFullWarp, ws, o);
+        const int v2 = __shfl_xor_sync(kFullWarp, wv, o);
+        wn += __shfl_xor_sync(kFullWarp, wn, o);
+        row_combine(wm, wv, ws, m2, v2, s2, c2, has_p);
+        const float b2 = __shfl_xor_sync(kFullWarp, wb, o);
+        const int bv2 = __shfl_xor_sync(kFullWarp, wbv, o);
+        arg_combine(wb, wbv, b2, bv2);
       }
-      const unsigned excl = incl - (c0 + c1 + cc2 + c3);
-      const unsigned kk = unsigned(k);
-      int j = -1;
-      if (excl < kk && incl >= kk) {
-        unsigned cum = excl + c0;
-        j = cum >= kk ? 4 * lane
-                      : ((cum += c1) >= kk ? 4 * lane + 1
-                                           : ((cum += cc2) >= kk ? 4 * lane + 2 : 4 * lane + 3));
+      ov = __any_sync(kFullWarp, ov != 0);
+      er = __any_sync(kFullWarp, er != 0);
+      if (lane == 0) {
+        s_f[0] = wm;
+        s_f[1] = ws;
+        s_i[0] = wv;
+        s_i[1] = wn;
+        s_i[2] = wbv;
+        s_i[3] = ov | (er << 1);
       }
-      const unsigned found = __ballot_sync(kFullWarp, j >= 0);
-      j = __shfl_sync(kFullWarp, j, found ? __ffs(found) - 1 : 0);
-      if (lane == 0) s_i[2] = found ? j : -1;
     }
     __syncthreads();
-    jk = s_i[2];
-  }
-  float fcut = fm;  // certified lower bound of the keep-threshold
-  if (jk >= 0 && jk < kKBins - 1) fcut = fmaxf(fcut, __fsub_rd(lmax, kbin_hi(jk)));
-  if (has_p) {
-    float D = logf(float(ncand_ub) / (fmaxf(1.f - tp, 1e-30f) * S));
-    D = fmaxf(D, 0.f) * 1.001f + 1e-3f;
-    fcut = fmaxf(fcut, __fsub_rd(lmax, T * D));
-  }
-  // the buffer holds every candidate in [lo_w, lmax]
-  const float lo_w = has_m ? fm : __fsub_ru(lmax, delta);
+    const float lmax = s_f[0];
+    const float S = s_f[1];
+    const int larg = s_i[0];
+    const int ncand_ub = s_i[1];  // candidates counted by their bits (-inf included)
+    const bool row_err = (s_i[3] >> 1) != 0;
 
-  // ------------------------------------ radix select of the threshold
-  unsigned long long P = 0ull;  // fixed-point top-p mass target
-  if (has_p) {
-    const float t = fmaxf(tp, 0.f) * S * 1099511627776.0f;
-    P = t >= 1.8e19f ? ~0ull : static_cast<unsigned long long>(t);
-  }
-  int npass = 0;
-  // Largest key x >= key(lo) with count(>= x) >= k (top-k) or mass(>= x) >= P
-  // (top-p), counting candidates of the buffer or of a fresh stream of the part.
-  // False when none exists.
-  auto descend = [&](bool from_buffer, float lo, uint32_t& out_key) -> bool {
-    const uint32_t klo = fkey(lo), khi = fkey(lmax);
-    const uint32_t diff = klo ^ khi;
-    int top = diff ? 32 - __clz(diff) : kLow + 1;  // one past the highest differing bit
-    top = max(top, kLow + 1);
-    int shift = max(top - 8, kLow);
-    uint32_t prefix = top >= 32 ? 0u : khi & ~((1u << top) - 1u);
-    unsigned above_c = 0;
-    unsigned long long above_m = 0;
-    for (;;) {
-      const int hp = npass & 1;
-      ++npass;
-      hist.cnt[hp][tid] = 0u;
-      hist.mass[hp][tid] = 0ull;
-      if (tid == 0) s_sel = -1;
-      __syncthreads();
-      const uint32_t himask = top >= 32 ? 0u : ~((1u << top) - 1u);
-      const uint32_t dmask = (1u << (top - shift)) - 1u;
-      // warp-uniform: every lane calls with its element (or part = false)
-      auto add = [&](float x, bool part) {
-        int d = -1;
-        if (part && x >= lo) {
-          const uint32_t kx = fkey(x);
-          if (((kx ^ prefix) & himask) == 0u) d = int((kx >> shift) & dmask);
-        }
-        if (!__any_sync(kFullWarp, d >= 0)) return;
-        const unsigned peers = __match_any_sync(kFullWarp, d);
-        if (d < 0) return;
-        const bool leader = lane == __ffs(peers) - 1;
-        if (has_p) {
-          const float e = exp2f((x - lmax) * c2);
-          const unsigned long long mm = __float2ull_rn(e * 1099511627776.0f);
-          const unsigned hi = __reduce_add_sync(peers, unsigned(mm >> 20));
-          const unsigned lw = __reduce_add_sync(peers, unsigned(mm & 0xFFFFFu));
-          if (leader)
-            atomicAdd(&hist.mass[hp][d], (static_cast<unsigned long long>(hi) << 20) + lw);
-        }
-        if (leader) atomicAdd(&hist.cnt[hp][d], unsigned(__popc(peers)));
-      };
-      bool ok = true;
-      if (from_buffer) {
-        for (int b0 = warp * 32; b0 < nbuf; b0 += kThreads) {
-          const int i = b0 + lane;
-          add(i < nbuf ? bval[i] : 0.f, i < nbuf);
-        }
-      } else {
-        ok = stream(
-            [&](int, bool, const uint4& raw, uint32_t cb, int) {
-              if (!__any_sync(kFullWarp, cb != 0)) return;
-#pragma unroll
-              for (int e = 0; e < EPV; ++e) {
-                const float x = E::get(raw, e);
-                add(x, ((cb >> e) & 1u) && x > -INFINITY);
-              }
-            },
-            []() {});
-      }
-      (void)ok;
-      __syncthreads();
-      xsync();
-      // bin tid summed over the cluster, then a descending inclusive scan
-      unsigned c = 0;
-      unsigned long long mass = 0;
+    if (row_err || lmax == -INFINITY || greedy || unfiltered) {
+      if (rank == 0 && tid == 0)
+        a.out[row] = row_err ? -2
+                     : lmax == -INFINITY ? -1
+                     : greedy ? larg
+                              : (s_i[2] == INT_MAX ? -1 : s_i[2]);
+      continue;
+    }
+    const bool any_overflow = (s_i[3] & 1) != 0;
+    const int nbuf = min(s_count, kCap);
+
+    // ------------------------------------------------------- filter bounds
+    if (k > 0 && k >= ncand_ub) k = 0;  // keeps every candidate
+    const bool has_k = k > 0;
+    const float fm = has_m ? fminf(__fadd_ru(lmax, tl), lmax) : -INFINITY;
+    // top-k: the k-th largest per-thread maximum of the cluster bounds t_k from below
+    int jk = -1;
+    if (has_k && k <= C * kThreads) {
       for (int r = 0; r < C; ++r) {
-        const Hist* h = cluster.map_shared_rank(&hist, r);
-        c += h->cnt[hp][tid];
-        mass += h->mass[hp][tid];
+        const float v = cluster.map_shared_rank(&tmaxs[par][0], r)[tid];
+        if (v > -INFINITY) atomicAdd(&kmerge[kbin(lmax - v)], 1u);
       }
-      unsigned sc = c;
-      unsigned long long smass = mass;
+      __syncthreads();
+      if (warp == 0) {
+        const unsigned c0 = kmerge[4 * lane], c1 = kmerge[4 * lane + 1];
+        const unsigned cc2 = kmerge[4 * lane + 2], c3 = kmerge[4 * lane + 3];
+        unsigned incl = c0 + c1 + cc2 + c3;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned yc = __shfl_down_sync(kFullWarp, sc, o);
-        const unsigned long long ym = __shfl_down_sync(kFullWarp, smass, o);
-        if (lane + o < 32) {
-          sc += yc;
-          smass += ym;
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned y = __shfl_up_sync(kFullWarp, incl, o);
+          if (lane >= o) incl += y;
         }
+        const unsigned excl = incl - (c0 + c1 + cc2 + c3);
+        const unsigned kk = unsigned(k);
+        int j = -1;
+        if (excl < kk && incl >= kk) {
+          unsigned cum = excl + c0;
+          j = cum >= kk ? 4 * lane
+                        : ((cum += c1) >= kk ? 4 * lane + 1
+                                             : ((cum += cc2) >= kk ? 4 * lane + 2 : 4 * lane + 3));
+        }
+        const unsigned found = __ballot_sync(kFullWarp, j >= 0);
+        j = __shfl_sync(kFullWarp, j, found ? __ffs(found) - 1 : 0);
+        if (lane == 0) s_i[2] = found ? j : -1;
+      }
+      __syncthreads();
+      jk = s_i[2];
+    }
+    float fcut = fm;  // certified lower bound of the keep-threshold
+    if (jk >= 0 && jk < kKBins - 1) fcut = fmaxf(fcut, __fsub_rd(lmax, kbin_hi(jk)));
+    if (has_p) {
+      float D = logf(float(ncand_ub) / (fmaxf(1.f - tp, 1e-30f) * S));
+      D = fmaxf(D, 0.f) * 1.001f + 1e-3f;
+      fcut = fmaxf(fcut, __fsub_rd(lmax, T * D));
+    }
+    // the buffer holds every candidate in [lo_w, lmax]
+    const float lo_w = has_m ? fm : __fsub_ru(lmax, delta);
+
+    // Re-reads this CTA's part from global memory (the ring is prefetching the
+    // next row): f(raw, cb, i0) per vector, warp-uniform.
+    auto reread = [&](auto&& f) {
+      for (int base = 0; base < pt.nvec; base += kThreads) {
+        const int q = base + tid;
+        int i0 = 0;
+        uint32_t cb = 0;
+        uint4 raw = make_uint4(0, 0, 0, 0);
+        if (q < pt.nvec) {
+          cb = pt.bits(q, i0, nullptr, 0, 0);
+          if (cb) raw = pt.gvec(q);
+        }
+        f(raw, cb, i0);
+      }
+    };
+
+    // ---------------------------------- radix select of the threshold
+    unsigned long long P = 0ull;  // fixed-point top-p mass target
+    if (has_p) {
+      const float t = fmaxf(tp, 0.f) * S * 1099511627776.0f;
+      P = t >= 1.8e19f ? ~0ull : static_cast<unsigned long long>(t);
+    }
+    // Largest key x >= key(lo) with count(>= x) >= k (top-k) or mass(>= x) >= P
+    // (top-p), counting candidates of the buffer or of a re-read of the part.
+    // False when none exists.
+    auto descend = [&](bool from_buffer, float lo, uint32_t& out_key) -> bool {
+      const uint32_t klo = fkey(lo), khi = fkey(lmax);
+      const uint32_t diff = klo ^ khi;
+      int top = diff ? 32 - __clz(diff) : kLow + 1;  // one past the highest differing bit
+      top = max(top, kLow + 1);
+      int shift = max(top - 8, kLow);
+      uint32_t prefix = top >= 32 ? 0u : khi & ~((1u << top) - 1u);
+      unsigned above_c = 0;
+      unsigned long long above_m = 0;
+      for (;;) {
+        const int hp = npass & 1;
+        ++npass;
+        hist.cnt[hp][tid] = 0u;
+        hist.mass[hp][tid] = 0ull;
+        if (tid == 0) s_sel = -1;
+        __syncthreads();
+        const uint32_t himask = top >= 32 ? 0u : ~((1u << top) - 1u);
+        const uint32_t dmask = (1u << (top - shift)) - 1u;
+        // warp-uniform: every lane calls with its element (or part = false)
+        auto add = [&](float x, bool part) {
+          int d = -1;
+          if (part && x >= lo) {
+            const uint32_t kx = fkey(x);
+            if (((kx ^ prefix) & himask) == 0u) d = int((kx >> shift) & dmask);
+          }
+          if (!__any_sync(kFullWarp, d >= 0)) return;
+          const unsigned peers = __match_any_sync(kFullWarp, d);
+          if (d < 0) return;
+          const bool leader = lane == __ffs(peers) - 1;
+          if (has_p) {
+            const float e = exp2f((x - lmax) * c2);
+            const unsigned long long mm = __float2ull_rn(e * 1099511627776.0f);
+            const unsigned hi = __reduce_add_sync(peers, unsigned(mm >> 20));
+            const unsigned lw = __reduce_add_sync(peers, unsigned(mm & 0xFFFFFu));
+            if (leader)
+              atomicAdd(&hist.mass[hp][d], (static_cast<unsigned long long>(hi) << 20) + lw);
+          }
+          if (leader) atomicAdd(&hist.cnt[hp][d], unsigned(__popc(peers)));
+        };
+        if (from_buffer) {
+          for (int b0 = warp * 32; b0 < nbuf; b0 += kThreads) {
+            const int i = b0 + lane;
+            add(i < nbuf ? bval[i] : 0.f, i < nbuf);
+          }
+        } else {
+          reread([&](const uint4& raw, uint32_t cb, int) {
+            if (!__any_sync(kFullWarp, cb != 0)) return;
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) {
+              const float x = E::get(raw, e);
+              add(x, ((cb >> e) & 1u) && x > -INFINITY);
+            }
+          });
+        }
+        __syncthreads();
+        xsync();
+        // bin tid summed over the cluster, then a descending inclusive scan
+        unsigned c = 0;
+        unsigned long long mass = 0;
+        for (int r = 0; r < C; ++r) {
+          const Hist* h = cluster.map_shared_rank(&hist, r);
+          c += h->cnt[hp][tid];
+          mass += h->mass[hp][tid];
+        }
+        unsigned sc = c;
+        unsigned long long smass = mass;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned yc = __shfl_down_sync(kFullWarp, sc, o);
+          const unsigned long long ym = __shfl_down_sync(kFullWarp, smass, o);
+          if (lane + o < 32) {
+            sc += yc;
+            smass += ym;
+          }
+        }
+        if (lane == 0) {
+          scan_c[warp] = sc;
+          scan_m[warp] = smass;
+        }
+        __syncthreads();
+        for (int w = warp + 1; w < kWarps; ++w) {
+          sc += scan_c[w];
+          smass += scan_m[w];
+        }
+        const unsigned cc = above_c + sc;
+        const unsigned long long cm = above_m + smass;
+        const bool okb = cc > 0u && ((has_k && cc >= unsigned(k)) || (has_p && cm >= P));
+        if (okb) atomicMax(&s_sel, tid);
+        __syncthreads();
+        const int sel = s_sel;
+        if (sel < 0) return false;
+        if (tid == sel) {
+          s_above_c = cc - c;
+          s_above_m = cm - mass;
+        }
+        __syncthreads();
+        above_c = s_above_c;
+        above_m = s_above_m;
+        prefix |= uint32_t(sel) << shift;
+        if (shift == kLow) {
+          out_key = prefix;
+          return true;
+        }
+        top = shift;
+        shift = max(top - 8, kLow);
+      }
+    };
+
+    float thr = fm;
+    bool from_buffer = !any_overflow;
+    const float lo_b = fmaxf(lo_w, fcut);
+    if (has_k || has_p) {
+      uint32_t kx = 0;
+      bool found = false;
+      if (from_buffer) {
+        found = descend(true, lo_b, kx);
+        if (!found && !(fm >= lo_b)) from_buffer = false;
+      }
+      if (!from_buffer) found = descend(false, fcut, kx);
+      if (found) thr = fmaxf(key_float(kx), fm);
+    } else if (from_buffer && !(fm >= lo_w)) {
+      from_buffer = false;
+    }
+
+    // ----------------------------------------------------------------- draw
+    best = -INFINITY;
+    bestv = INT_MAX;
+    if (from_buffer) {
+      for (int i = tid; i < nbuf; i += kThreads) {
+        const float x = bval[i];
+        if (!(x >= thr)) continue;
+        uint4 w;
+        int g = -1;
+        const int v = bidx[i];
+        arg_combine(best, bestv, score_of(__fdiv_rn(x, T), v, w, g), v);
+      }
+    } else {
+      wgrp = -1;
+      reread([&](const uint4& raw, uint32_t cb, int i0) {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+          const float x = E::get(raw, e);
+          if (!((cb >> e) & 1u) || !(x >= thr) || !(x > -INFINITY)) continue;
+          const float z = __fdiv_rn(x, T);
+          if (z + kGumbelMax < best) continue;
+          const int v = pt.start + i0 + e;
+          arg_combine(best, bestv, score_of(z, v, w4, wgrp), v);
+        }
+      });
+    }
+    {
+      float wb = best;
+      int wbv = bestv;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const float b2 = __shfl_xor_sync(kFullWarp, wb, o);
+        const int bv2 = __shfl_xor_sync(kFullWarp, wbv, o);
+        arg_combine(wb, wbv, b2, bv2);
       }
       if (lane == 0) {
-        scan_c[warp] = sc;
-        scan_m[warp] = smass;
+        red_b[warp] = wb;
+        red_bv[warp] = wbv;
       }
-      __syncthreads();
-      for (int w = warp + 1; w < kWarps; ++w) {
-        sc += scan_c[w];
-        smass += scan_m[w];
-      }
-      const unsigned cc = above_c + sc;
-      const unsigned long long cm = above_m + smass;
-      const bool okb = cc > 0u && ((has_k && cc >= unsigned(k)) || (has_p && cm >= P));
-      if (okb) atomicMax(&s_sel, tid);
-      __syncthreads();
-      const int sel = s_sel;
-      if (sel < 0) return false;
-      if (tid == sel) {
-        s_above_c = cc - c;
-        s_above_m = cm - mass;
-      }
-      __syncthreads();
-      above_c = s_above_c;
-      above_m = s_above_m;
-      prefix |= uint32_t(sel) << shift;
-      if (shift == kLow) {
-        out_key = prefix;
-        return true;
-      }
-      top = shift;
-      shift = max(top - 8, kLow);
     }
-  };
-
-  float thr = fm;
-  bool from_buffer = !any_overflow;
-  const float lo_b = fmaxf(lo_w, fcut);
-  if (has_k || has_p) {
-    uint32_t kx = 0;
-    bool found = false;
-    if (from_buffer) {
-      found = descend(true, lo_b, kx);
-      if (!found && !(fm >= lo_b)) from_buffer = false;
+    __syncthreads();
+    if (tid == 0) {
+      float wb = -INFINITY;
+      int wbv = INT_MAX;
+      for (int w = 0; w < kWarps; ++w) arg_combine(wb, wbv, red_b[w], red_bv[w]);
+      xchg[par].best = wb;
+      xchg[par].best_v = wbv;
     }
-    if (!from_buffer) found = descend(false, fcut, kx);
-    if (found) thr = fmaxf(key_float(kx), fm);
-  } else if (from_buffer && !(fm >= lo_w)) {
-    from_buffer = false;
+    xsync();
+    if (rank == 0 && tid == 0) {
+      float wb = -INFINITY;
+      int wbv = INT_MAX;
+      for (int r = 0; r < C; ++r) {
+        const Xchg* p = cluster.map_shared_rank(&xchg[par], r);
+        arg_combine(wb, wbv, p->best, p->best_v);
+      }
+      a.out[row] = wbv == INT_MAX ? -1 : wbv;
+    }
   }
 
-  // ------------------------------------------------------------------- draw
-  best = -INFINITY;
-  bestv = INT_MAX;
-  if (from_buffer) {
-    for (int i = tid; i < nbuf; i += kThreads) {
-      const float x = bval[i];
-      if (!(x >= thr)) continue;
-      uint4 w;
-      int g = -1;
-      const int v = bidx[i];
-      arg_combine(best, bestv, score_of(__fdiv_rn(x, T), v, w, g), v);
-    }
-  } else {
-    wgrp = -1;
-    stream(
-        [&](int, bool, const uint4& raw, uint32_t cb, int i0) {
-#pragma unroll
-          for (int e = 0; e < EPV; ++e) {
-            const float x = E::get(raw, e);
-            if (!((cb >> e) & 1u) || !(x >= thr) || !(x > -INFINITY)) continue;
-            const float z = __fdiv_rn(x, T);
-            if (z + kGumbelMax < best) continue;
-            const int v = pt.start + i0 + e;
-            arg_combine(best, bestv, score_of(z, v, w4, wgrp), v);
-          }
-        },
-        []() {});
-  }
-  {
-    float wb = best;
-    int wbv = bestv;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float b2 = __shfl_xor_sync(kFullWarp, wb, o);
-      const int bv2 = __shfl_xor_sync(kFullWarp, wbv, o);
-      arg_combine(wb, wbv, b2, bv2);
-    }
-    if (lane == 0) {
-      red_b[warp] = wb;
-      red_bv[warp] = wbv;
-    }
-  }
-  const int late_err = __syncthreads_or(s_err != 0);
-  if (tid == 0) {
-    float wb = -INFINITY;
-    int wbv = INT_MAX;
-    for (int w = 0; w < kWarps; ++w) arg_combine(wb, wbv, red_b[w], red_bv[w]);
-    xchg.best = wb;
-    xchg.best_v = late_err ? -2 : wbv;
-  }
-  xsync();
-  if (rank == 0 && tid == 0) {
-    float wb = -INFINITY;
-    int wbv = INT_MAX;
-    bool bad = false;
-    for (int r = 0; r < C; ++r) {
-      const Xchg* p = cluster.map_shared_rank(&xchg, r);
-      if (p->best_v == -2) bad = true;
-      arg_combine(wb, wbv, p->best, p->best_v);
-    }
-    a.out[row] = bad ? -2 : (wbv == INT_MAX ? -1 : wbv);
-  }
-  leave();
+  // Leave only once every stage is idle and the peers are done reading this
+  // CTA: a stage whose wait timed out gets one more bounded wait.
+  for (int sl = 0; sl < kRing; ++sl)
+    if ((lost >> sl) & 1u) (void)mbar_wait(&full[sl], (lost >> (sl + 8)) & 1u);
+  if (C > 1) cluster.sync();
 }
 
 __global__ void philox_kernel(const uint32_t* __restrict__ ctr, const uint32_t* __restrict__ key,
@@ -960,11 +990,11 @@ int64_t chunk_for(int64_t V, int S) {
   return std::max<int64_t>(c, 32);
 }
 
-// Split rows over more CTAs while the batch alone gives fewer than about three
-// CTAs per SM (the resident count), keeping at least 4096 tokens per CTA.
+// CTAs per row: one, unless there are fewer rows than SMs; then rows are split
+// over clusters until every SM has work, keeping at least 4096 tokens per CTA.
 int split_for(int64_t B, int64_t V) {
   int S = 1;
-  while (S < kMaxSplit && B * S < 3 * int64_t(num_sms()) && chunk_for(V, 2 * S) >= 4096) S *= 2;
+  while (S < kMaxSplit && B * S < int64_t(num_sms()) && chunk_for(V, 2 * S) >= 4096) S *= 2;
   return S;
 }
 
@@ -972,7 +1002,9 @@ template <int DT>
 cudaError_t launch_sample(SampleArgs a, int64_t B, int64_t V, cudaStream_t s) {
   static std::mutex mu;
   static bool configured = false;
-  const int S = split_for(B, V);
+  static std::map<int, int> clusters;  // resident clusters by cluster size
+  int S = split_for(B, V);
+  int resident = 0;
   {
     std::lock_guard<std::mutex> lock(mu);
     if (!configured) {
@@ -984,10 +1016,37 @@ cudaError_t launch_sample(SampleArgs a, int64_t B, int64_t V, cudaStream_t s) {
       if (e != cudaSuccess) return e;
       configured = true;
     }
+    for (;;) {
+      auto it = clusters.find(S);
+      if (it == clusters.end()) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(unsigned(S) * 64u);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = size_t(kSmem);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = unsigned(S);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, sample_kernel<DT>, &cfg) != cudaSuccess) {
+          (void)cudaGetLastError();
+          n = 0;
+        }
+        it = clusters.emplace(S, n).first;
+      }
+      resident = it->second;
+      if (resident > 0 || S == 1) break;
+      S /= 2;  // this cluster shape cannot be co-scheduled: try a smaller one
+    }
   }
+  if (resident <= 0) resident = std::max(1, 3 * num_sms() / S);
   a.chunk = int(chunk_for(V, S));
+  a.ncl = int(std::min<int64_t>(B, resident));
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(B) * unsigned(S));
+  cfg.gridDim = dim3(unsigned(a.ncl) * unsigned(S));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = size_t(kSmem);
   cfg.stream = s;

@@ -307,6 +307,25 @@ def test_long_rows():
             assert np.array_equal(got, want), (B, V, args)
 
 
+def test_small_rows_after_large_rows():
+    """Rows with fewer vectors than threads, sampled right after a launch that
+    leaves large logits in the staging shared memory: lanes without a vector
+    must contribute nothing (a cut of -inf once admitted them)."""
+    rng = np.random.default_rng(14)
+    big = to_dev(syn.to_storage((rng.standard_normal((3, 1_500_000)) * 8).astype(np.float32),
+                                "bf16"), "bf16")
+    V = 64
+    x = np.tile((rng.standard_normal(V) * 1.5).astype(np.float32), (20_000, 1))
+    xt = torch.from_numpy(x).cuda()
+    for args in (dict(temperature=0.7, top_k=10), dict(temperature=1.2, top_p=0.8),
+                 dict(temperature=1.0, min_p=0.1), dict(temperature=1.0)):
+        ops.sample(big, seed=1, temperature=1.0, top_k=100)
+        g = ops.sample(xt, seed=99, offset=5, **args).cpu().numpy()
+        want = oracle.mask_and_sample(x, dtype=oracle.F32, seed=99, offset=5, **args)
+        assert ((g >= 0) & (g < V)).all(), args
+        assert (g == want).mean() >= 0.999, args
+
+
 # ---------------------------------------------------- distribution, determinism
 
 def test_distribution_same_streams_and_exact():
