@@ -125,8 +125,8 @@ __device__ __forceinline__ void row_combine(float& m, int& v, float& s, float m2
                                             float c2, bool with_sum) {
   if (with_sum) {
     const float M = fmaxf(m, m2);
-    const float a = m > -INFINITY ? s * exp2f((m - M) * c2) : 0.f;
-    const float b = m2 > -INFINITY ? s2 * exp2f((m2 - M) * c2) : 0.f;
+    const float a = m > -INFINITY ? s * ex2((m - M) * c2) : 0.f;
+    const float b = m2 > -INFINITY ? s2 * ex2((m2 - M) * c2) : 0.f;
     s = a + b;
   }
   arg_combine(m, v, m2, v2);
@@ -328,6 +328,7 @@ __global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleArgs a)
   __shared__ unsigned long long s_above_m;
   __shared__ int s_masked[2];  // masked flag of the row of each parity
   __shared__ __align__(8) uint64_t full[kRing];
+  __shared__ uint4 keep_tab[256];  // 16-bit types: per-word keep masks of 8 element bits
   __shared__ int4 pmeta[kRing];  // per slot: vectors [x, y), staged mask words [z, w)
   __shared__ int pwhole[kRing];  // per slot: every vector of the piece is a whole vector
 
@@ -336,6 +337,8 @@ __global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleArgs a)
     for (int r = 0; r < kRing; ++r) mbar_init(&full[r], 1);
     mbar_init_fence();
   }
+  keep_tab[tid] = make_uint4(keep_mask16(tid, 0), keep_mask16(tid, 1), keep_mask16(tid, 2),
+                             keep_mask16(tid, 3));
   __syncthreads();
 
   const uint2 key = make_uint2(uint32_t(a.seed), uint32_t(a.seed >> 32));
@@ -380,14 +383,18 @@ __global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleArgs a)
       bulk_load(ring + slot * kPieceBytes + 16 * (v0 - q0), g.g0 + 16 * v0, vbytes, &full[slot]);
     if (mbytes) bulk_load(mring + slot * kMaskSlot, g.gmask + m_lo, mbytes, &full[slot]);
   };
+  __shared__ Pt pg;  // producer: geometry of row p_iter (thread 0 only)
+  int pg_iter = -1;  // the iteration pg describes
   auto top_up = [&](int cur) {  // thread 0 only
     while (issued - consumed < uint32_t(kRing)) {
       const int prow = row_of(p_iter);
       if (prow >= a.B || p_iter > cur + 1) break;
-      Pt g;
-      g.init(a, prow, rank, s_masked[p_iter & 1] != 0);
-      if (p_piece < g.npieces) {
-        issue(g, p_piece);
+      if (pg_iter != p_iter) {
+        pg.init(a, prow, rank, s_masked[p_iter & 1] != 0);
+        pg_iter = p_iter;
+      }
+      if (p_piece < pg.npieces) {
+        issue(pg, p_piece);
         ++p_piece;
       } else {
         ++p_iter;
@@ -472,12 +479,25 @@ __global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleArgs a)
       const bool whole = pwhole[slot] != 0;
       const unsigned char* data = ring + slot * kPieceBytes;
       const uint32_t* mw = reinterpret_cast<const uint32_t*>(mring + slot * kMaskSlot);
-      // vector q of this piece and its candidate bits
+      // vector q of this piece, its candidate bits, and (16-bit types) the vector
+      // with every non-candidate element replaced by -inf
       auto load = [&](int q, uint4& raw, uint32_t& cb) {
         const bool staged = whole || (q >= pt.qf0 && q < pt.qf1);
         raw = staged ? *reinterpret_cast<const uint4*>(data + 16 * (q - pm.x)) : pt.gvec(q);
         int i0;
         cb = (whole && !pt.masked) ? Pt::ALL : pt.bits(q, i0, mw, pm.z, pm.w);
+      };
+      auto masked_vec = [&](const uint4& raw, uint32_t cb) -> uint4 {
+        if (cb == Pt::ALL) return raw;
+        if (Pt::EB == 4) {
+          constexpr uint32_t kNegInf = 0xff800000u;
+          return make_uint4((cb & 1u) ? raw.x : kNegInf, (cb & 2u) ? raw.y : kNegInf,
+                            (cb & 4u) ? raw.z : kNegInf, (cb & 8u) ? raw.w : kNegInf);
+        }
+        const uint32_t ninf2 = DT == LP_BF16 ? 0xff80ff80u : 0xfc00fc00u;
+        const uint4 t = keep_tab[cb];
+        return make_uint4((raw.x & t.x) | (ninf2 & ~t.x), (raw.y & t.y) | (ninf2 & ~t.y),
+                          (raw.z & t.z) | (ninf2 & ~t.z), (raw.w & t.w) | (ninf2 & ~t.w));
       };
       float vms[kPerPiece];
 #pragma unroll
@@ -489,26 +509,26 @@ __global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleArgs a)
         uint32_t cb;
         load(q, raw, cb);
         if (!cb) continue;
-        const float vm = VecMax<DT>::run(raw, cb);
+        const uint4 mv = masked_vec(raw, cb);
+        const float vm = VecMax<DT>::run(mv, Pt::ALL);
         vms[r] = vm;
         cnt += __popc(cb);
         if (vm > m) {
-          if (has_p && m > -INFINITY) sm *= exp2f((m - vm) * c2);
+          if (has_p) sm *= ex2((m - vm) * c2);  // 0 while m is still -inf
           m = vm;
           mq = q;
         }
-        if (has_p) {
+        if (has_p && vm > -INFINITY) {  // m is finite: -inf elements add 0
           const float off = m * c2;
 #pragma unroll
-          for (int e = 0; e < EPV; ++e)
-            if ((cb >> e) & 1u) sm += exp2f(fmaf(E::get(raw, e), c2, -off));
+          for (int e = 0; e < EPV; ++e) sm += ex2(fmaf(E::get(mv, e), c2, -off));
         }
         if (unfiltered) {
           const int i0 = (16 * q - pt.mis) / Pt::EB;
 #pragma unroll
           for (int e = 0; e < EPV; ++e) {
-            const float x = E::get(raw, e);
-            if (!((cb >> e) & 1u) || !(x > -INFINITY)) continue;
+            const float x = E::get(mv, e);
+            if (!(x > -INFINITY)) continue;
             const float z = __fdiv_rn(x, T);
             if (z + kGumbelMax < best) continue;  // cannot win
             const int v = pt.start + i0 + e;
@@ -698,7 +718,7 @@ __global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleArgs a)
     const float fm = has_m ? fminf(__fadd_ru(lmax, tl), lmax) : -INFINITY;
     // top-k: the k-th largest per-thread maximum of the cluster bounds t_k from below
     int jk = -1;
-    if (has_k && k <= C * kThreads) {
+    if (has_k && !has_m && k <= C * kThreads) {
       for (int r = 0; r < C; ++r) {
         const float v = cluster.map_shared_rank(&tmaxs[par][0], r)[tid];
         if (v > -INFINITY) atomicAdd(&kmerge[kbin(lmax - v)], 1u);
@@ -794,7 +814,7 @@ __global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleArgs a)
           if (d < 0) return;
           const bool leader = lane == __ffs(peers) - 1;
           if (has_p) {
-            const float e = exp2f((x - lmax) * c2);
+            const float e = ex2((x - lmax) * c2);
             const unsigned long long mm = __float2ull_rn(e * 1099511627776.0f);
             const unsigned hi = __reduce_add_sync(peers, unsigned(mm >> 20));
             const unsigned lw = __reduce_add_sync(peers, unsigned(mm & 0xFFFFFu));
