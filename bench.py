@@ -228,6 +228,12 @@ class Op:
         self.params = {k: torch.from_numpy(w.per_row(k)).to(dev)
                        for k in ("temperature", "top_k", "top_p", "min_p")}
         self.out = torch.empty(w.B, dtype=torch.int64, device=dev)
+        # one zero-filled sampler workspace for every replay (the kernels leave it zeroed)
+        self.ws = None
+        if kind == "sample":
+            tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.dtype]
+            self.ws = torch.zeros(max(1, ops.sample_workspace_bytes(tdt, w.B, w.cols)),
+                                  dtype=torch.uint8, device=dev)
         self.bytes = touched
         self.units = w.B
 
@@ -243,7 +249,7 @@ class Op:
                                 seed=w.seed, offset=w.offsets[step % len(w.offsets)],
                                 indices=self.indices,
                                 vocab_size=w.vocab_size if bm is not None else None,
-                                out=self.out)
+                                out=self.out, workspace=self.ws)
 
     def capture(self, nsteps: int, first_step: int):
         torch = self.torch

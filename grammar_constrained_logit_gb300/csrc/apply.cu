@@ -121,22 +121,28 @@ __global__ void __launch_bounds__(kApplyThreads) apply_kernel(const ApplyArgs a)
          j += blockDim.x)
       scalar(j);
 
-    // whole vectors of this block's vector range
+    // whole vectors of this block's vector range: every mask word, then every
+    // logits vector that must be read, then the stores, so that one thread's
+    // loads are all in flight together (a store may alias a later load, which
+    // would otherwise hold that load back behind it)
+    int64_t j0[kVecPerThread];
+    uint32_t keep[kVecPerThread];
 #pragma unroll
     for (int k = 0; k < kVecPerThread; ++k) {
       const int64_t q = int64_t(blockIdx.x) * kVecPerBlock + k * kApplyThreads + threadIdx.x;
-      if (q >= nvec) break;
-      const int64_t j0 = head + q * EPV;
-      const uint32_t keep = sel ? mask_bits(mrow, j0, EPV, limit) : ALL;
-      if (!OOP && keep == ALL) continue;
-      uint4 v;
-      if (keep == 0u)
-        v = fill_v;
-      else if (keep == ALL)
-        v = ld_stream(rin + j0 * EB);
-      else
-        v = E::blend(ld_stream(rin + j0 * EB), keep, a.fill);
-      st_stream(rout + j0 * EB, v);
+      j0[k] = head + q * EPV;
+      keep[k] = q >= nvec ? ~0u : sel ? mask_bits(mrow, j0[k], EPV, limit) : ALL;
+    }
+    uint4 v[kVecPerThread];
+#pragma unroll
+    for (int k = 0; k < kVecPerThread; ++k)
+      if (keep[k] != ~0u && keep[k] != 0u && (OOP || keep[k] != ALL))
+        v[k] = ld_stream(rin + j0[k] * EB);
+#pragma unroll
+    for (int k = 0; k < kVecPerThread; ++k) {
+      if (keep[k] == ~0u || (!OOP && keep[k] == ALL)) continue;
+      const uint4 w = keep[k] == 0u ? fill_v : keep[k] == ALL ? v[k] : E::blend(v[k], keep[k], a.fill);
+      st_stream(rout + j0[k] * EB, w);
     }
   }
 }

@@ -2,79 +2,119 @@
 // sampler (Kernel Hub "logits-processor", Ops "sample" and "How it works";
 // unsatisfiable rows as in TensorRT-Edge-LLM "Guided Decoder").
 //
-// GB300 design: one streaming pass over HBM through the Tensor Memory
-// Accelerator, in a persistent grid.  A row is split over a thread-block cluster
-// of S CTAs; the resident clusters take the rows round-robin.  Each CTA streams
-// its parts of its rows through a ring of four 8 KB shared-memory stages: one
-// thread keeps bulk copies (cp.async.bulk, with the stage's bitmask words) in
-// flight on mbarriers, running up to one row ahead, so the next row's loads
-// overlap this row's reductions; the 256 threads consume each landed stage from
-// shared memory.  The CTAs of a row combine partial results through distributed
-// shared memory (DSMEM) behind cluster barriers; nothing is written to global
-// memory but the ids.
+// GB300 design: two kernels per call.
 //
-// Per row, in the stream:
-//   * candidate max, the vector holding it (its lowest index is found after the
-//     pass), the candidate count and, for top-p rows, an online softmax sum;
-//   * filtered rows: every candidate within a window below the running maximum
-//     (shared by the CTA's warps through a shared-memory atomicMax) is appended
-//     to a compaction buffer.  The window is exactly the min-p bound when min-p is
-//     on (max + T ln min_p); otherwise a number of temperature units growing with
-//     ln(1 / (1 - top_p)) for top-p and a fixed number of logits for top-k.  The
-//     running maximum never exceeds the row maximum, so the buffer holds every
-//     candidate in [max - window, max];
+// The stream kernel makes the one pass over HBM, through the Tensor Memory
+// Accelerator, in a persistent grid of three CTAs per SM.  Every row is cut into
+// tiles of equal length (8-32 KB of logits) and the CTAs take the tiles of all
+// rows round-robin, so the work per SM is even whatever the batch size and
+// vocabulary.  A CTA streams its tiles through a ring of four 8 KB
+// shared-memory stages: one thread keeps bulk copies (cp.async.bulk, with the
+// stage's bitmask words) in flight on mbarriers, running up to one tile ahead,
+// and the 256 threads consume each landed stage from shared memory.  Per tile:
+//   * candidate max with its lowest index, the candidate count and, for top-p
+//     rows, an online softmax sum;
+//   * filtered rows: every candidate within a window below the tile's running
+//     maximum is appended to a shared-memory compaction buffer.  The window is
+//     exactly the min-p bound when min-p is on (max + T ln min_p); otherwise a
+//     number of temperature units growing with ln(1 / (1 - top_p)) for top-p and
+//     a fixed number of logits for top-k.  No tile maximum exceeds the row
+//     maximum, so the tiles' buffers together hold every candidate in
+//     [row max - window, row max];
 //   * rows without filters draw Gumbel-max directly (no threshold needed),
 //     skipping any token whose best possible score is below the running best.
-// After the stream (one exchange): no candidate -> -1; greedy -> argmax;
-// unfiltered -> the best score's token.  Filtered rows find the keep-threshold
-// max(t_k, t_p, t_m) by an MSD radix select over the order-preserving key of the
-// logit -- counts for top-k and 2^-40 fixed-point softmax mass for top-p, pre-summed
-// per warp (match_any + redux) and summed over the cluster per digit; one descent
-// serves both filters: the threshold is the largest key at which "count >= k" or
-// "mass >= top_p S" first holds.  The descent runs on the buffer, counting only the
-// region where the buffer is complete; if the threshold is not found there (or a
-// buffer overflowed) the CTAs stream their parts again (an L2 hit in practice) and
-// select and draw from those.  The draw is Gumbel-max over the kept set with
-// Philox4x32-10 noise keyed by (seed, row, offset).
-// Masses are integers, so every cluster-wide sum is exact and order-independent;
-// the softmax sum is reduced in a fixed order.  Results are deterministic in
-// (seed, offset).
-#include <cooperative_groups.h>
-
+// The tile's summary and buffer go to a caller-provided device workspace with
+// plain stores: the buffer to the tile's own slot, or -- when longer than a
+// slot -- to a shared pool.  Nothing in the stream waits on another CTA.
+//
+// The finish kernel (one CTA per row, launched as a programmatic dependent of
+// the stream kernel so that its launch overlaps the stream) merges the row's
+// tile summaries: no candidate -> -1; greedy -> argmax; unfiltered -> the best
+// score's token.  Filtered rows find the keep-threshold max(t_k, t_p, t_m) by
+// an MSD radix select over the order-preserving key of the logit -- counts for
+// top-k and 2^-40 fixed-point softmax mass for top-p, pre-summed per warp
+// (match_any + redux); one descent serves both filters: the threshold is the
+// largest key at which "count >= k" or "mass >= top_p S" first holds.  The
+// descent reads the tiles' buffers (L2 resident), counting only the region where
+// they are complete; if the threshold is not there (or a buffer overflowed) the
+// CTA reads the whole row again and selects and draws from that.  The draw is
+// Gumbel-max over the kept set with Philox4x32-10 noise keyed by
+// (seed, row, offset).
+// Masses are integers, so every sum over tiles or warps is exact and
+// order-independent; softmax sums are merged in a fixed order.  Results are
+// deterministic in (seed, offset).
 #include <algorithm>
 #include <climits>
 #include <cmath>
-#include <map>
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
-
-namespace cg = cooperative_groups;
 
 namespace lp {
 namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kConsumerWarps = kWarps - 1;  // stream kernel: the last warp is the producer
+constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kRing = 4;                 // stages in flight per CTA
-constexpr int kPieceBytes = 8192;        // bytes of logits per stage
+constexpr int kPieceBytes = 7168;        // bytes of logits per stage: two vectors per consumer
 constexpr int kPieceWords = kPieceBytes / 2 / 32 + 2;  // bitmask words a stage can need
 constexpr int kMaskSlot = (16 + 4 * kPieceWords + 15) / 16 * 16;
-constexpr int kPerPiece = kPieceBytes / 16 / 256;  // vectors of a piece per thread
-constexpr int kKBins = 128;              // log-spaced bins of (row max - thread max)
-constexpr int kKBase = (127 - 6) << 3;   // code of 2^-6 (8 exponent + 3 fraction bits)
-constexpr int kMaxSplit = 16;
-constexpr int kCap = 3072;               // compaction entries per CTA
+constexpr int kPerPiece = kPieceBytes / 16 / kConsumers;  // vectors of a piece per consumer
+static_assert(kPerPiece * 16 * kConsumers == kPieceBytes, "a piece is whole vectors per consumer");
+constexpr int kTileBytesMax = 32768;     // longest tile
+constexpr int kTileBytesMin = 8192;      // shortest tile (small batches)
+constexpr int64_t kTileTarget = 1024;    // tiles per launch that shorter tiles aim for
+constexpr int kCap = 3072;               // compaction entries per tile (shared memory)
+constexpr int kSlotCap = 256;            // entries a tile keeps in its own workspace slot
+constexpr int kStage = 4096;             // buffered entries a finishing CTA stages
+constexpr int kMetaCap = 1024;           // tiles per row whose buffer starts it stages
+constexpr int kFinishSmem = kStage * 8 + (kMetaCap + 1) * 4;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kWindowK = 6.f;          // top-k window, in logits
 constexpr int kSmem = kRing * kPieceBytes + kRing * kMaskSlot + kCap * 8;
 constexpr uint32_t kMaxWaitTries = 1u << 22;
+constexpr int64_t kMaxTileSums = int64_t(1) << 20;  // tiles per launch
+constexpr int64_t kMaxRowsPerLaunch = 16384;
+constexpr int64_t kPoolPerRow = 8192;    // pooled compaction entries per row
+constexpr int64_t kPoolMin = int64_t(1) << 16;
+constexpr int64_t kPoolMax = int64_t(1) << 24;
+constexpr uint32_t kTileOverflow = 1u << 30;
+// row modes of the stream kernel's piece loop
+constexpr int kModeGreedy = 0;      // max and argmax only
+constexpr int kModeTopP = 1;        // + softmax sum and the compaction buffer
+constexpr int kModeFilter = 2;      // + the compaction buffer (top-k, min-p)
+constexpr int kModeUnfiltered = 3;  // + Gumbel-max in the stream
+constexpr uint32_t kTileError = 1u << 31;
+
+// ------------------------------------------------------------ workspace
+
+struct WsHeader {       // one per workspace
+  unsigned pool_used;   // pool entries handed out by the running stream kernel
+  unsigned pad[63];
+};
+struct TileSum {  // one per tile of a launch
+  float max;
+  int arg;    // lowest index of max
+  float sum;  // softmax sum relative to max (top-p rows)
+  int ncand;  // candidate bits seen (-inf logits included)
+  float best;
+  int best_v;     // unfiltered rows: best Gumbel score and its token
+  unsigned off;   // buffer longer than a slot: pool entries [off, off + n)
+  unsigned nf;    // n | kTileOverflow | kTileError
+};
 
 struct SampleArgs {
   const char* logits;
   int64_t stride_bytes;
-  int B;
   int V;
+  int row0;   // first row of this launch
+  int nrows;  // rows in this launch
+  int tpr;    // tiles per row
+  int chunk;  // tokens per tile (a multiple of 32)
+  int64_t ntiles;
   const uint32_t* bitmask;  // nullptr: no row is masked
   int64_t bm_stride;
   int64_t bm_rows;
@@ -90,20 +130,82 @@ struct SampleArgs {
   float minp_s;
   uint64_t seed, offset;
   int64_t* out;
-  int chunk;  // tokens per CTA (a multiple of 32)
-  int ncl;    // clusters in the grid; cluster c owns rows c, c + ncl, ...
+  WsHeader* hdr;
+  unsigned* rowkey;  // [rows]: largest published running maximum per row (order key; 0 none)
+  TileSum* ts;     // [ntiles]
+  float* slot_val;  // [ntiles, kSlotCap]
+  int* slot_idx;
+  float* pool_val;  // [pool_cap]
+  int* pool_idx;
+  unsigned pool_cap;
 };
 
-struct Xchg {  // per-CTA values read by the other CTAs of the cluster
-  float max;
-  int arg;
-  float sum;  // softmax sum relative to max
-  int ncand;
-  int overflow;
-  int err;
-  float best;
-  int best_v;
+// One row's sampling parameters and what follows from them.
+struct RowParams {
+  float T, tp, mp;
+  int k;
+  bool greedy, has_p, has_m, has_k0, unfiltered, compact;
+  float c2;     // log2(e) / T
+  float tl;     // min-p bound below the maximum: max + tl
+  float delta;  // compaction window below the running maximum
 };
+
+struct RawParams {
+  float T, tp, mp;
+  int k;
+};
+__device__ __forceinline__ RawParams raw_params(const SampleArgs& a, int row) {
+  RawParams p;
+  p.T = a.temp ? a.temp[row] : a.temp_s;
+  p.k = a.topk ? a.topk[row] : a.topk_s;
+  p.tp = a.topp ? a.topp[row] : a.topp_s;
+  p.mp = a.minp ? a.minp[row] : a.minp_s;
+  return p;
+}
+__device__ __forceinline__ RowParams row_params(const RawParams& p) {
+  RowParams r;
+  r.T = p.T;
+  r.k = p.k;
+  r.tp = p.tp;
+  r.mp = p.mp;
+  r.greedy = !(r.T > 0.f) || r.k == 1;
+  r.has_p = !r.greedy && r.tp < 1.f;
+  r.has_m = !r.greedy && r.mp > 0.f;
+  r.has_k0 = !r.greedy && r.k > 0;
+  r.unfiltered = !r.greedy && !r.has_p && !r.has_m && !r.has_k0;
+  r.compact = !r.greedy && !r.unfiltered;
+  r.c2 = r.greedy ? 0.f : kLog2e / r.T;
+  r.tl = r.has_m ? r.T * logf(r.mp) : 0.f;
+  float d = INFINITY;
+  if (r.has_m) d = fminf(d, -r.tl);
+  if (r.has_p) d = fminf(d, r.T * (2.f + 2.5f * logf(1.f / fmaxf(1.f - r.tp, 1e-6f))));
+  if (r.has_k0) d = fminf(d, kWindowK);
+  r.delta = d > 0.f ? d : 0.f;
+  return r;
+}
+
+// Gumbel score of candidate token v of row with z = x / T; w4/wgrp cache v's
+// Philox block.
+__device__ __forceinline__ float gumbel_score(float z, int v, int row, uint64_t offset,
+                                             uint2 key, uint4& w4, int& wgrp) {
+  const int grp = v >> 2;
+  if (grp != wgrp) {
+    w4 = philox4x32_10(
+        make_uint4(uint32_t(grp), uint32_t(row), uint32_t(offset), uint32_t(offset >> 32)), key);
+    wgrp = grp;
+  }
+  const uint32_t word = (v & 3) == 0 ? w4.x : (v & 3) == 1 ? w4.y : (v & 3) == 2 ? w4.z : w4.w;
+  return z + gumbel_from_word(word);
+}
+
+// Programmatic dependent launch: wait for the grid this one depends on, and let
+// the next grid in the stream begin its launch.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
 
 struct Hist {  // radix histograms, double-buffered by pass parity
   unsigned long long mass[2][256];
@@ -117,7 +219,7 @@ __device__ __forceinline__ void arg_combine(float& s, int& v, float s2, int v2) 
   }
 }
 
-// Merge two partial row summaries (max, lowest index of the max and -- when
+// Merge two partial summaries (max, lowest index of the max and -- when
 // with_sum -- the sum of exp2((x - max) c2)).  Symmetric in its two arguments, so
 // a butterfly leaves the same value in every lane and any fixed merge order is
 // deterministic.
@@ -130,17 +232,6 @@ __device__ __forceinline__ void row_combine(float& m, int& v, float& s, float m2
     s = a + b;
   }
   arg_combine(m, v, m2, v2);
-}
-
-// Log-spaced bin of d >= 0: bin 0 holds d < 2^-6, then 8 bins per octave; the
-// last bin also takes everything larger.
-__device__ __forceinline__ int kbin(float d) {
-  const int code = int(__float_as_uint(d) >> 20);
-  return min(max(code - kKBase + 1, 0), kKBins - 1);
-}
-// Exclusive upper edge of bin j (j < kKBins - 1).
-__device__ __forceinline__ float kbin_hi(int j) {
-  return j == 0 ? 0.015625f : __uint_as_float(unsigned(j + kKBase) << 20);
 }
 
 // ------------------------------------------------------ TMA and mbarriers
@@ -190,29 +281,31 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
-// ------------------------------------------------------------ row part
+// -------------------------------------------------------------- row span
 
-// One CTA's part of one row: local element i is token start + i, at byte
-// mis + i * EB of a 16-byte aligned window starting at g0.  The window is
-// streamed in pieces of kPieceBytes.  Whole 16-byte vectors [qf0, qf1) of the
-// window arrive by bulk copy; the ragged first and last vectors are read from
-// global memory when used.  Each piece's bitmask words arrive with it: words
-// [m_lo, m_hi) (relative to the part) sit at byte mmis + 4 (w - m_lo) of the
-// piece's mask slot; other words are read from global memory.
+// A contiguous span of one row (a tile, or the whole row): local element i is
+// token start + i, at byte mis + i * EB of a 16-byte aligned window starting at
+// g0.  The window is streamed in pieces of kPieceBytes.  Whole 16-byte vectors
+// [qf0, qf1) of the window arrive by bulk copy; the ragged first and last
+// vectors are read from global memory when used.  Each piece's bitmask words
+// arrive with it: words [m_lo, m_hi) (relative to the span) sit at byte
+// 4 (w - m_lo) of the piece's mask slot; other words are read from global
+// memory.
 template <int DT>
-struct Part {
+struct Span {
   using E = Elt<DT>;
   static constexpr int EPV = E::kPerVec;
   static constexpr int EB = E::kBytes;
   static constexpr uint32_t ALL = (1u << EPV) - 1u;
   const char* g0;
-  const uint32_t* gmask;  // the part's bitmask words (masked rows)
+  const uint32_t* gmask;  // the span's bitmask words (masked rows)
   int start, n_local, mis, win, nvec, nwords, qf0, qf1, npieces;
   bool masked;
 
-  __device__ __forceinline__ void init(const SampleArgs& a, int row, int rank, bool m) {
-    start = rank * a.chunk;
-    n_local = max(0, min(a.chunk, a.V - start));
+  // tokens [s, s + n) of row (s a multiple of 32)
+  __device__ __forceinline__ void init(const SampleArgs& a, int row, int s, int n, bool m) {
+    start = s;
+    n_local = max(0, n);
     const char* gsrc = a.logits + int64_t(row) * a.stride_bytes + int64_t(start) * EB;
     mis = int(reinterpret_cast<uintptr_t>(gsrc) & 15);
     g0 = gsrc - mis;
@@ -224,6 +317,11 @@ struct Part {
     npieces = n_local ? (win + kPieceBytes - 1) / kPieceBytes : 0;
     masked = m;
     gmask = m ? a.bitmask + int64_t(row) * a.bm_stride + (start >> 5) : nullptr;
+  }
+  // tile `part` of row
+  __device__ __forceinline__ void init_tile(const SampleArgs& a, int row, int part, bool m) {
+    const int s = part * a.chunk;
+    init(a, row, s, min(a.chunk, a.V - s), m);
   }
   // vectors [q0, q1) of piece j
   __device__ __forceinline__ void piece_vecs(int j, int& q0, int& q1) const {
@@ -239,16 +337,13 @@ struct Part {
     w0 = i0 >> 5;
     w1 = i1 > i0 ? ((i1 - 1) >> 5) + 1 : w0;
   }
-  // the 16-byte aligned interior [m_lo, m_hi) of words [w0, w1), and the byte
-  // offset of word m_lo in its slot
-  __device__ __forceinline__ void mask_interior(int w0, int w1, int& m_lo, int& m_hi,
-                                                int& mmis) const {
+  // the 16-byte aligned interior [m_lo, m_hi) of words [w0, w1)
+  __device__ __forceinline__ void mask_interior(int w0, int w1, int& m_lo, int& m_hi) const {
     const uintptr_t a0 = reinterpret_cast<uintptr_t>(gmask + w0);
     const int lead = int(((16 - (a0 & 15)) & 15) >> 2);
     m_lo = min(w0 + lead, w1);
     const uintptr_t a1 = reinterpret_cast<uintptr_t>(gmask + w1) & ~uintptr_t(15);
     m_hi = max(m_lo, int((a1 - reinterpret_cast<uintptr_t>(gmask)) >> 2));
-    mmis = 0;
   }
   __device__ __forceinline__ uint4 gvec(int q) const {  // from global memory
     if (q >= qf0 && q < qf1) return __ldg(reinterpret_cast<const uint4*>(g0 + 16 * q));
@@ -266,8 +361,8 @@ struct Part {
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
   }
-  // candidate bits of vector q (element e a token of this part kept by the mask),
-  // its mask words taken from `mw` (words [m_lo, m_hi)) or global memory
+  // candidate bits of vector q (element e a token of this span kept by the
+  // mask), its mask words taken from `mw` (words [m_lo, m_hi)) or global memory
   __device__ __forceinline__ uint32_t bits(int q, int& i0, const uint32_t* mw, int m_lo,
                                            int m_hi) const {
     i0 = (16 * q - mis) / EB;
@@ -289,24 +384,43 @@ struct Part {
   }
 };
 
-template <int DT>
-__global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleArgs a) {
-  using E = Elt<DT>;
-  using Pt = Part<DT>;
-  constexpr int EPV = E::kPerVec;
-  constexpr int kLow = int(E::kLowKeyBit);
+// Rows listed in the call's indices (every row when there is no list) are
+// masked; block-uniform, every thread of the block calls it.
+__device__ __forceinline__ bool row_masked(const SampleArgs& a, int row) {
+  if (!a.bitmask) return false;
+  if (a.indices == nullptr) return true;
+  int found = 0;
+  for (int i = threadIdx.x; i < a.n_indices; i += blockDim.x) found |= (a.indices[i] == row);
+  return __syncthreads_or(found) != 0 && row < a.bm_rows;
+}
 
-  cg::cluster_group cluster = cg::this_cluster();
-  const int C = int(cluster.num_blocks());
-  const int rank = int(cluster.block_rank());
-  const int cid = int(blockIdx.x) / C;
+// ================================================================ stream kernel
+
+// Consumer-only barriers (named barrier 1; the producer warp never joins).
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;\n" ::"n"(kConsumers) : "memory");
+}
+__device__ __forceinline__ int consumer_sync_or(int pred) {
+  int r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.s32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n"
+      " selp.s32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(pred), "n"(kConsumers)
+      : "memory");
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* m) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(m)) : "memory");
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const SampleArgs a) {
+  using E = Elt<DT>;
+  using Sp = Span<DT>;
+  constexpr int EPV = E::kPerVec;
+
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  auto xsync = [&]() {
-    if (C > 1)
-      cluster.sync();
-    else
-      __syncthreads();
-  };
 
   extern __shared__ __align__(16) unsigned char smem[];
   unsigned char* const ring = smem;
@@ -314,289 +428,305 @@ __global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleArgs a)
   float* const bval = reinterpret_cast<float*>(mring + kRing * kMaskSlot);
   int* const bidx = reinterpret_cast<int*>(bval + kCap);
 
-  __shared__ Xchg xchg[2];              // by row parity: read by peers without a trailing barrier
-  __shared__ float tmaxs[2][kThreads];  // per-thread maxima, by row parity
-  __shared__ Hist hist;                 // by radix-pass parity
-  __shared__ float red_f[kWarps], red_s[kWarps], red_b[kWarps];
-  __shared__ int red_i[kWarps], red_n[kWarps], red_bv[kWarps];
-  __shared__ unsigned scan_c[kWarps];
-  __shared__ unsigned long long scan_m[kWarps];
-  __shared__ unsigned kmerge[kKBins];
-  __shared__ int s_count, s_sel, s_err, s_i[4];
-  __shared__ float s_f[3];
-  __shared__ unsigned s_runkey, s_above_c;
-  __shared__ unsigned long long s_above_m;
-  __shared__ int s_masked[2];  // masked flag of the row of each parity
+  __shared__ float red_f[kConsumerWarps], red_s[kConsumerWarps], red_b[kConsumerWarps];
+  __shared__ int red_i[kConsumerWarps], red_n[kConsumerWarps], red_bv[kConsumerWarps];
+  __shared__ int s_count, s_err;
+  __shared__ unsigned s_off, s_nf;
+  __shared__ unsigned s_runkey;
   __shared__ __align__(8) uint64_t full[kRing];
+  __shared__ __align__(8) uint64_t empty[kRing];
   __shared__ uint4 keep_tab[256];  // 16-bit types: per-word keep masks of 8 element bits
-  __shared__ int4 pmeta[kRing];  // per slot: vectors [x, y), staged mask words [z, w)
-  __shared__ int pwhole[kRing];  // per slot: every vector of the piece is a whole vector
+  __shared__ int4 pmeta[kRing];    // per slot: vectors [x, y), staged mask words [z, w)
+  __shared__ int pflag[kRing];     // per slot: bit 0 whole vectors only, bit 1 row masked
 
   if (tid == 0) {
     s_err = 0;
-    for (int r = 0; r < kRing; ++r) mbar_init(&full[r], 1);
+    for (int r = 0; r < kRing; ++r) {
+      mbar_init(&full[r], 1);
+      mbar_init(&empty[r], kConsumerWarps);
+    }
     mbar_init_fence();
   }
   keep_tab[tid] = make_uint4(keep_mask16(tid, 0), keep_mask16(tid, 1), keep_mask16(tid, 2),
                              keep_mask16(tid, 3));
+  // The finish kernel may begin its launch now; its blocks wait for this grid
+  // to complete before they read anything.  This grid in turn waits for the
+  // previous one in the stream before its first global read.
+  launch_dependents();
+  grid_dependency_wait();
   __syncthreads();
 
-  const uint2 key = make_uint2(uint32_t(a.seed), uint32_t(a.seed >> 32));
-  auto row_of = [&](int it) { return cid + it * a.ncl; };
-  auto masked_of = [&](int row) -> bool {  // block-uniform
-    if (!a.bitmask) return false;
-    if (a.indices == nullptr) return true;
-    int found = 0;
-    for (int i = tid; i < a.n_indices; i += kThreads) found |= (a.indices[i] == row);
-    return __syncthreads_or(found) != 0 && row < a.bm_rows;
-  };
+  const int64_t G = gridDim.x;
+  auto tile_of = [&](int it) { return int64_t(blockIdx.x) + it * G; };
+  auto row_of = [&](int64_t t) { return a.row0 + int(t / a.tpr); };
+  auto part_of = [&](int64_t t) { return int(t % a.tpr); };
 
-  // ---------------------------------------------------------------- the ring
-  // Pieces of this CTA's rows are copied in row order into slot (n % kRing) of
-  // the n-th piece; thread 0 keeps up to kRing of them in flight, at most one
-  // row ahead of the row being consumed, so the next row's loads overlap this
-  // row's reductions.
-  uint32_t issued = 0, consumed = 0, lost = 0;
-  int p_iter = 0, p_piece = 0;  // producer position (thread 0)
-  auto issue = [&](const Pt& g, int j) {
-    const int slot = int(issued % kRing);
-    ++issued;
-    int q0, q1;
-    g.piece_vecs(j, q0, q1);
-    const int v0 = max(q0, g.qf0), v1 = min(q1, g.qf1);
-    const uint32_t vbytes = v1 > v0 ? uint32_t(16 * (v1 - v0)) : 0u;
-    uint32_t mbytes = 0;
-    int w0 = 0, w1 = 0, m_lo = 0, m_hi = 0, mmis = 0;
-    if (g.masked) {
-      g.piece_words(j, w0, w1);
-      g.mask_interior(w0, w1, m_lo, m_hi, mmis);
-      mbytes = uint32_t(4 * (m_hi - m_lo));
-    }
-    pmeta[slot] = make_int4(q0, q1, m_lo, m_hi);  // published by the arrive below
-    pwhole[slot] = q0 >= g.qf0 && q1 <= g.qf1;
-    if (s_err) {  // a copy went missing earlier: start no more (rows report -2)
-      mbar_expect_tx(&full[slot], 0);
-      return;
-    }
-    mbar_expect_tx(&full[slot], vbytes + mbytes);
-    if (vbytes)
-      bulk_load(ring + slot * kPieceBytes + 16 * (v0 - q0), g.g0 + 16 * v0, vbytes, &full[slot]);
-    if (mbytes) bulk_load(mring + slot * kMaskSlot, g.gmask + m_lo, mbytes, &full[slot]);
-  };
-  __shared__ Pt pg;  // producer: geometry of row p_iter (thread 0 only)
-  int pg_iter = -1;  // the iteration pg describes
-  auto top_up = [&](int cur) {  // thread 0 only
-    while (issued - consumed < uint32_t(kRing)) {
-      const int prow = row_of(p_iter);
-      if (prow >= a.B || p_iter > cur + 1) break;
-      if (pg_iter != p_iter) {
-        pg.init(a, prow, rank, s_masked[p_iter & 1] != 0);
-        pg_iter = p_iter;
+  // ================================================================ producer
+  // Warp kConsumerWarps copies the pieces of this CTA's tiles, in order, into
+  // ring slot (n % kRing) of the n-th piece: it waits until the consumers have
+  // released the slot, publishes the piece's geometry and starts its bulk
+  // copies on the slot's mbarrier.
+  if (warp == kConsumerWarps) {
+    uint32_t issued = 0;
+    for (int it = 0; tile_of(it) < a.ntiles; ++it) {
+      const int64_t tile = tile_of(it);
+      const int row = row_of(tile);
+      bool masked = false;  // warp-uniform
+      if (a.bitmask) {
+        if (a.indices == nullptr) {
+          masked = true;
+        } else {
+          int found = 0;
+          for (int i = lane; i < a.n_indices; i += 32) found |= (a.indices[i] == row);
+          masked = __any_sync(kFullWarp, found) && row < a.bm_rows;
+        }
       }
-      if (p_piece < pg.npieces) {
-        issue(pg, p_piece);
-        ++p_piece;
-      } else {
-        ++p_iter;
-        p_piece = 0;
+      Sp g;
+      g.init_tile(a, row, part_of(tile), masked);
+      for (int j = 0; j < g.npieces; ++j, ++issued) {
+        const int slot = int(issued % kRing);
+        if (issued >= uint32_t(kRing) &&
+            !mbar_wait(&empty[slot], ((issued / kRing) - 1u) & 1u) && lane == 0)
+          s_err = 1;  // the consumers are gone: copy nothing more
+        if (lane != 0) continue;
+        int q0, q1;
+        g.piece_vecs(j, q0, q1);
+        const int v0 = max(q0, g.qf0), v1 = min(q1, g.qf1);
+        const uint32_t vbytes = v1 > v0 ? uint32_t(16 * (v1 - v0)) : 0u;
+        uint32_t mbytes = 0;
+        int m_lo = 0, m_hi = 0;
+        if (g.masked) {
+          int w0, w1;
+          g.piece_words(j, w0, w1);
+          g.mask_interior(w0, w1, m_lo, m_hi);
+          mbytes = uint32_t(4 * (m_hi - m_lo));
+        }
+        pmeta[slot] = make_int4(q0, q1, m_lo, m_hi);  // published by the arrive below
+        pflag[slot] = (q0 >= g.qf0 && q1 <= g.qf1 ? 1 : 0) | (g.masked ? 2 : 0);
+        if (*(volatile int*)&s_err) {  // a copy went missing: start no more (rows report -2)
+          mbar_expect_tx(&full[slot], 0);
+          continue;
+        }
+        mbar_expect_tx(&full[slot], vbytes + mbytes);
+        if (vbytes)
+          bulk_load(ring + slot * kPieceBytes + 16 * (v0 - q0), g.g0 + 16 * v0, vbytes,
+                    &full[slot]);
+        if (mbytes) bulk_load(mring + slot * kMaskSlot, g.gmask + m_lo, mbytes, &full[slot]);
       }
     }
-  };
-
-  if (row_of(0) < a.B) {
-    const bool m0 = masked_of(row_of(0));
-    if (tid == 0) s_masked[0] = m0;
+    return;
   }
-  int npass = 0;  // radix passes so far: histogram parity
 
-  for (int it = 0; row_of(it) < a.B; ++it) {
-    const int row = row_of(it);
-    const int par = it & 1;
-    __syncthreads();  // the previous row is done in this CTA
-    if (row_of(it + 1) < a.B) {
-      const bool mn = masked_of(row_of(it + 1));
-      if (tid == 0) s_masked[par ^ 1] = mn;
-    }
+  // =============================================================== consumers
+  const uint2 key = make_uint2(uint32_t(a.seed), uint32_t(a.seed >> 32));
+  uint32_t consumed = 0, lost = 0;
+  RawParams nxt{};  // the next tile's row parameters, loaded a tile ahead
+  if (tile_of(0) < a.ntiles) nxt = raw_params(a, row_of(tile_of(0)));
+
+  for (int it = 0; tile_of(it) < a.ntiles; ++it) {
+    const int64_t tile = tile_of(it);
+    const int row = row_of(tile);
+    const int lrow = row - a.row0;
+    consumer_sync();  // the previous tile's buffer is written out
     if (tid == 0) {
       s_count = 0;
-      s_runkey = fkey(-INFINITY);
+      s_runkey = 0u;
     }
-    if (tid < kKBins) kmerge[tid] = 0u;
-    __syncthreads();
-    if (tid == 0) top_up(it);
+    consumer_sync();
 
-    Pt pt;
-    pt.init(a, row, rank, s_masked[par] != 0);
-    const float T = a.temp ? a.temp[row] : a.temp_s;
-    int k = a.topk ? a.topk[row] : a.topk_s;
-    const float tp = a.topp ? a.topp[row] : a.topp_s;
-    const float mp = a.minp ? a.minp[row] : a.minp_s;
-    const bool greedy = !(T > 0.f) || k == 1;
-    const bool has_p = !greedy && tp < 1.f;
-    const bool has_m = !greedy && mp > 0.f;
-    const bool has_k0 = !greedy && k > 0;
-    const bool unfiltered = !greedy && !has_p && !has_m && !has_k0;
-    const bool compact = !greedy && !unfiltered;
-    const float c2 = greedy ? 0.f : kLog2e / T;
-    const float tl = has_m ? T * logf(mp) : 0.f;  // min-p bound below the maximum: max + tl
-    float delta = INFINITY;                       // compaction window below the running max
-    if (has_m) delta = fminf(delta, -tl);
-    if (has_p) delta = fminf(delta, T * (2.f + 2.5f * logf(1.f / fmaxf(1.f - tp, 1e-6f))));
-    if (has_k0) delta = fminf(delta, kWindowK);
-    if (!(delta > 0.f)) delta = 0.f;
+    Sp pt;
+    pt.init_tile(a, row, part_of(tile), false);  // masked: from the first piece
+    const RowParams rp = row_params(nxt);
+    if (tile_of(it + 1) < a.ntiles) nxt = raw_params(a, row_of(tile_of(it + 1)));
+    const float T = rp.T, c2 = rp.c2, delta = rp.delta;
+    // the largest running maximum the row's other tiles have published, read one
+    // piece ahead of its use (thread 0)
+    unsigned hint = 0u;
 
-    // Gumbel score of candidate (z = x / T, token v); w4/wgrp cache v's Philox block
-    auto score_of = [&](float z, int v, uint4& w4, int& wgrp) {
-      const int grp = v >> 2;
-      if (grp != wgrp) {
-        w4 = philox4x32_10(make_uint4(uint32_t(grp), uint32_t(row), uint32_t(a.offset),
-                                      uint32_t(a.offset >> 32)),
-                           key);
-        wgrp = grp;
-      }
-      const uint32_t word = (v & 3) == 0 ? w4.x : (v & 3) == 1 ? w4.y : (v & 3) == 2 ? w4.z : w4.w;
-      return z + gumbel_from_word(word);
-    };
-
-    // ------------------------------------------------- stream the row part
+    // ------------------------------------------------------ stream the tile
     float m = -INFINITY, sm = 0.f;  // running max and softmax sum relative to it
-    int mq = -1, cnt = 0;           // vector of the running max; candidate bits seen
+    int targ = INT_MAX, cnt = 0;    // lowest index of the running max; candidate bits seen
     float best = -INFINITY;         // unfiltered rows: running best score
     int bestv = INT_MAX;
     uint4 w4 = make_uint4(0, 0, 0, 0);
     int wgrp = -1;
     bool stream_ok = true;
-    for (int j = 0; j < pt.npieces; ++j) {
-      const int slot = int(consumed % kRing);
-      const uint32_t parity = (consumed / kRing) & 1u;
-      ++consumed;
-      if (!mbar_wait(&full[slot], parity)) {
-        stream_ok = false;
-        s_err = 1;
-        lost |= (1u << slot) | (parity << (slot + 8));
-      }
-      const int4 pm = pmeta[slot];
-      const bool whole = pwhole[slot] != 0;
-      const unsigned char* data = ring + slot * kPieceBytes;
-      const uint32_t* mw = reinterpret_cast<const uint32_t*>(mring + slot * kMaskSlot);
-      // vector q of this piece, its candidate bits, and (16-bit types) the vector
-      // with every non-candidate element replaced by -inf
-      auto load = [&](int q, uint4& raw, uint32_t& cb) {
-        const bool staged = whole || (q >= pt.qf0 && q < pt.qf1);
-        raw = staged ? *reinterpret_cast<const uint4*>(data + 16 * (q - pm.x)) : pt.gvec(q);
-        int i0;
-        cb = (whole && !pt.masked) ? Pt::ALL : pt.bits(q, i0, mw, pm.z, pm.w);
-      };
-      auto masked_vec = [&](const uint4& raw, uint32_t cb) -> uint4 {
-        if (cb == Pt::ALL) return raw;
-        if (Pt::EB == 4) {
-          constexpr uint32_t kNegInf = 0xff800000u;
-          return make_uint4((cb & 1u) ? raw.x : kNegInf, (cb & 2u) ? raw.y : kNegInf,
-                            (cb & 4u) ? raw.z : kNegInf, (cb & 8u) ? raw.w : kNegInf);
+    // The piece loop, compiled once per row mode so that each mode's loop holds
+    // only its own work.
+    auto stream = [&](auto mode_tag) {
+      constexpr int kMode = decltype(mode_tag)::value;
+      constexpr bool has_p = kMode == kModeTopP;
+      constexpr bool unfiltered = kMode == kModeUnfiltered;
+      constexpr bool compact = kMode == kModeTopP || kMode == kModeFilter;
+      for (int j = 0; j < pt.npieces; ++j) {
+        const int slot = int(consumed % kRing);
+        const uint32_t parity = (consumed / kRing) & 1u;
+        ++consumed;
+        if (!mbar_wait(&full[slot], parity)) {
+          stream_ok = false;
+          s_err = 1;
+          lost |= (1u << slot) | (parity << (slot + 8));
         }
-        const uint32_t ninf2 = DT == LP_BF16 ? 0xff80ff80u : 0xfc00fc00u;
-        const uint4 t = keep_tab[cb];
-        return make_uint4((raw.x & t.x) | (ninf2 & ~t.x), (raw.y & t.y) | (ninf2 & ~t.y),
-                          (raw.z & t.z) | (ninf2 & ~t.z), (raw.w & t.w) | (ninf2 & ~t.w));
-      };
-      float vms[kPerPiece];
-#pragma unroll
-      for (int r = 0; r < kPerPiece; ++r) {
-        const int q = pm.x + r * kThreads + tid;
-        vms[r] = -INFINITY;
-        if (q >= pm.y) continue;
-        uint4 raw;
-        uint32_t cb;
-        load(q, raw, cb);
-        if (!cb) continue;
-        const uint4 mv = masked_vec(raw, cb);
-        const float vm = VecMax<DT>::run(mv, Pt::ALL);
-        vms[r] = vm;
-        cnt += __popc(cb);
-        if (vm > m) {
-          if (has_p) sm *= ex2((m - vm) * c2);  // 0 while m is still -inf
-          m = vm;
-          mq = q;
+        const int4 pm = pmeta[slot];
+        const int pf = pflag[slot];
+        const bool whole = (pf & 1) != 0;
+        if (j == 0 && (pf & 2)) {
+          pt.masked = true;
+          pt.gmask = a.bitmask + int64_t(row) * a.bm_stride + (pt.start >> 5);
         }
-        if (has_p && vm > -INFINITY) {  // m is finite: -inf elements add 0
-          const float off = m * c2;
-#pragma unroll
-          for (int e = 0; e < EPV; ++e) sm += ex2(fmaf(E::get(mv, e), c2, -off));
-        }
-        if (unfiltered) {
-          const int i0 = (16 * q - pt.mis) / Pt::EB;
-#pragma unroll
-          for (int e = 0; e < EPV; ++e) {
-            const float x = E::get(mv, e);
-            if (!(x > -INFINITY)) continue;
-            const float z = __fdiv_rn(x, T);
-            if (z + kGumbelMax < best) continue;  // cannot win
-            const int v = pt.start + i0 + e;
-            arg_combine(best, bestv, score_of(z, v, w4, wgrp), v);
+        const unsigned char* data = ring + slot * kPieceBytes;
+        const uint32_t* mw = reinterpret_cast<const uint32_t*>(mring + slot * kMaskSlot);
+        // vector q of this piece and its candidate bits
+        const bool plain = whole && !pt.masked;  // every vector staged, every token a candidate
+        auto load = [&](int q, uint4& raw, uint32_t& cb) {
+          if (plain) {
+            raw = *reinterpret_cast<const uint4*>(data + 16 * (q - pm.x));
+            cb = Sp::ALL;
+            return;
           }
-        }
-      }
-      if (compact) {  // warp-uniform: append the piece's candidates within the window
-        float wm = m;
-#pragma unroll
-        for (int o = 16; o; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(kFullWarp, wm, o));
-        if (lane == 0 && wm > -INFINITY) atomicMax(&s_runkey, fkey(wm));
-        const float rm = fmaxf(wm, key_float(*(volatile unsigned*)&s_runkey));
-        const float cut = __fsub_rd(rm, delta);
+          const bool staged = whole || (q >= pt.qf0 && q < pt.qf1);
+          raw = staged ? *reinterpret_cast<const uint4*>(data + 16 * (q - pm.x)) : pt.gvec(q);
+          int i0;
+          cb = (whole && !pt.masked) ? Sp::ALL : pt.bits(q, i0, mw, pm.z, pm.w);
+        };
+        // the vector with every non-candidate element replaced by -inf
+        auto masked_vec = [&](const uint4& raw, uint32_t cb) -> uint4 {
+          if (cb == Sp::ALL) return raw;
+          if (Sp::EB == 4) {
+            constexpr uint32_t kNegInf = 0xff800000u;
+            return make_uint4((cb & 1u) ? raw.x : kNegInf, (cb & 2u) ? raw.y : kNegInf,
+                              (cb & 4u) ? raw.z : kNegInf, (cb & 8u) ? raw.w : kNegInf);
+          }
+          const uint32_t ninf2 = DT == LP_BF16 ? 0xff80ff80u : 0xfc00fc00u;
+          const uint4 t = keep_tab[cb];
+          return make_uint4((raw.x & t.x) | (ninf2 & ~t.x), (raw.y & t.y) | (ninf2 & ~t.y),
+                            (raw.z & t.z) | (ninf2 & ~t.z), (raw.w & t.w) | (ninf2 & ~t.w));
+        };
+        // every vector of the thread first (independent loads and maxima), then the
+        // running maximum once, then the softmax terms
+        uint4 mv[kPerPiece];
+        uint32_t cbs[kPerPiece];
+        float vms[kPerPiece];
 #pragma unroll
         for (int r = 0; r < kPerPiece; ++r) {
-          // a lane without a vector has vms = -inf, which must not pass a cut of -inf
-          const bool live = vms[r] > -INFINITY && vms[r] >= cut;
-          if (!__any_sync(kFullWarp, live)) continue;
-          const int q = pm.x + r * kThreads + tid;
-          uint32_t pass = 0;
+          const int q = pm.x + r * kConsumers + tid;
           uint4 raw = make_uint4(0, 0, 0, 0);
-          if (live) {
-            uint32_t cb;
-            load(q, raw, cb);
+          uint32_t cb = 0;
+          if (q < pm.y) load(q, raw, cb);
+          cbs[r] = cb;
+          mv[r] = masked_vec(raw, cb);
+          vms[r] = cb ? VecMax<DT>::run(mv[r], Sp::ALL) : -INFINITY;
+          cnt += __popc(cb);
+        }
+        float pmx = vms[0];
+        int rmx = 0;
 #pragma unroll
-            for (int e = 0; e < EPV; ++e) {
-              const float x = E::get(raw, e);
-              if (((cb >> e) & 1u) && x >= cut && x > -INFINITY) pass |= 1u << e;
-            }
+        for (int r = 1; r < kPerPiece; ++r)
+          if (vms[r] > pmx) {
+            pmx = vms[r];
+            rmx = r;
           }
-          const int n = __popc(pass);
-          int incl = n;
+        if (pmx > m) {  // a new running maximum: its lowest index in this piece
+          if constexpr (has_p) sm *= ex2((m - pmx) * c2);  // 0 while m is still -inf
+          m = pmx;
+          const int q = pm.x + rmx * kConsumers + tid;
+          const int i0 = (16 * q - pt.mis) / Sp::EB;
 #pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(kFullWarp, incl, o);
-            if (lane >= o) incl += y;
-          }
-          int pos = 0;
-          if (lane == 31) pos = atomicAdd(&s_count, incl);
-          pos = __shfl_sync(kFullWarp, pos, 31) + incl - n;
-          const int i0 = (16 * q - pt.mis) / Pt::EB;
-          while (pass) {
-            const int e = __ffs(pass) - 1;
-            pass &= pass - 1;
-            if (pos < kCap) {
-              bval[pos] = E::get(raw, e);
-              bidx[pos] = pt.start + i0 + e;
-            }
-            ++pos;
+          for (int e = EPV - 1; e >= 0; --e)
+            if (E::get(mv[rmx], e) == pmx) targ = pt.start + i0 + e;
+        }
+        if constexpr (has_p) {  // -inf elements add 0 (m is finite once any candidate is seen)
+          const float off = m * c2;
+#pragma unroll
+          for (int r = 0; r < kPerPiece; ++r) {
+            if (!cbs[r] || !(m > -INFINITY)) continue;
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) sm += ex2(fmaf(E::get(mv[r], e), c2, -off));
           }
         }
-      }
-      __syncthreads();  // every thread is done with the slot
-      if (tid == 0) top_up(it);
-    }
-
-    // -------------------------------------------------------- row summaries
-    tmaxs[par][tid] = m;
-    int targ = INT_MAX;
-    if (mq >= 0) {  // lowest index of the thread's maximum, in the first vector holding it
-      int i0;
-      const uint32_t cb = pt.bits(mq, i0, nullptr, 0, 0);
-      const uint4 raw = pt.gvec(mq);
+        if constexpr (unfiltered) {
 #pragma unroll
-      for (int e = EPV - 1; e >= 0; --e)
-        if (((cb >> e) & 1u) && E::get(raw, e) == m) targ = pt.start + i0 + e;
+          for (int r = 0; r < kPerPiece; ++r) {
+            if (!cbs[r]) continue;
+            const int q = pm.x + r * kConsumers + tid;
+            const int i0 = (16 * q - pt.mis) / Sp::EB;
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) {
+              const float x = E::get(mv[r], e);
+              if (!(x > -INFINITY)) continue;
+              const float z = __fdiv_rn(x, T);
+              if (z + kGumbelMax < best) continue;  // cannot win
+              const int v = pt.start + i0 + e;
+              arg_combine(best, bestv, gumbel_score(z, v, row, a.offset, key, w4, wgrp), v);
+            }
+          }
+        }
+        if constexpr (compact) {  // warp-uniform: append the piece's candidates within the window
+          float wm = m;
+#pragma unroll
+          for (int o = 16; o; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(kFullWarp, wm, o));
+          if (lane == 0 && wm > -INFINITY) atomicMax(&s_runkey, fkey(wm));
+          if (tid == 0) {  // exchange with the row's other tiles
+            if (j > 0 && hint) atomicMax(&s_runkey, hint);
+            const unsigned mine = *(volatile unsigned*)&s_runkey;
+            if (mine) atomicMax(&a.rowkey[lrow], mine);
+            hint = *(volatile unsigned*)&a.rowkey[lrow];
+          }
+          const unsigned rk = *(volatile unsigned*)&s_runkey;
+          const float rm = rk ? fmaxf(wm, key_float(rk)) : wm;
+          const float cut = __fsub_rd(rm, delta);
+#pragma unroll
+          for (int r = 0; r < kPerPiece; ++r) {
+            // a lane without a vector has vms = -inf, which must not pass a cut of -inf
+            const bool live = vms[r] > -INFINITY && vms[r] >= cut;
+            if (!__any_sync(kFullWarp, live)) continue;
+            const int q = pm.x + r * kConsumers + tid;
+            uint32_t pass = 0;
+            if (live) {
+#pragma unroll
+              for (int e = 0; e < EPV; ++e) {
+                const float x = E::get(mv[r], e);
+                if (x >= cut && x > -INFINITY) pass |= 1u << e;
+              }
+            }
+            const int n = __popc(pass);
+            int incl = n;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const int y = __shfl_up_sync(kFullWarp, incl, o);
+              if (lane >= o) incl += y;
+            }
+            int pos = 0;
+            if (lane == 31) pos = atomicAdd(&s_count, incl);
+            pos = __shfl_sync(kFullWarp, pos, 31) + incl - n;
+            const int i0 = (16 * q - pt.mis) / Sp::EB;
+            while (pass) {
+              const int e = __ffs(pass) - 1;
+              pass &= pass - 1;
+              if (pos < kCap) {
+                bval[pos] = E::get(mv[r], e);
+                bidx[pos] = pt.start + i0 + e;
+              }
+              ++pos;
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);  // this warp is done with the slot
+      }
+    };
+    switch (rp.greedy ? kModeGreedy
+            : rp.has_p ? kModeTopP
+            : rp.compact ? kModeFilter
+                         : kModeUnfiltered) {
+      case kModeGreedy: stream(std::integral_constant<int, kModeGreedy>{}); break;
+      case kModeTopP: stream(std::integral_constant<int, kModeTopP>{}); break;
+      case kModeFilter: stream(std::integral_constant<int, kModeFilter>{}); break;
+      default: stream(std::integral_constant<int, kModeUnfiltered>{}); break;
     }
+    const bool has_p = rp.has_p, unfiltered = rp.unfiltered, compact = rp.compact;
+
+    // ------------------------------------------------------- tile summary
     {
       float wm = m, ws = sm, wb = best;
       int wv = targ, wn = cnt, wbv = bestv;
@@ -622,11 +752,11 @@ __global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleArgs a)
         red_bv[warp] = wbv;
       }
     }
-    const int cta_err = __syncthreads_or(!stream_ok || s_err != 0);
+    const int cta_err = consumer_sync_or(!stream_ok || s_err != 0);
     if (warp == 0) {
       float wm = -INFINITY, ws = 0.f, wb = -INFINITY;
       int wv = INT_MAX, wn = 0, wbv = INT_MAX;
-      if (lane < kWarps) {
+      if (lane < kConsumerWarps) {
         wm = red_f[lane];
         ws = red_s[lane];
         wv = red_i[lane];
@@ -646,34 +776,166 @@ __global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleArgs a)
         arg_combine(wb, wbv, b2, bv2);
       }
       if (lane == 0) {
-        Xchg& x = xchg[par];
-        x.max = wm;
-        x.arg = wv;
-        x.sum = ws;
-        x.ncand = wn;
-        x.best = wb;
-        x.best_v = wbv;
-        x.overflow = s_count > kCap;
-        x.err = cta_err;
+        // the buffer goes to the tile's slot, or to the pool when longer
+        const unsigned n = compact ? unsigned(s_count) : 0u;
+        unsigned nf = n, off = 0u;
+        if (n > unsigned(kCap)) {
+          nf = kTileOverflow;
+        } else if (n > unsigned(kSlotCap)) {
+          off = atomicAdd(&a.hdr->pool_used, n);
+          if (off > a.pool_cap || n > a.pool_cap - off) nf = kTileOverflow;
+        }
+        if (cta_err) nf |= kTileError;
+        s_off = off;
+        s_nf = nf;
+        TileSum& t = a.ts[tile];
+        t.max = wm;
+        t.arg = wv;
+        t.sum = ws;
+        t.ncand = wn;
+        t.best = wb;
+        t.best_v = wbv;
+        t.off = off;
+        t.nf = nf;
+        if (compact && wm > -INFINITY) atomicMax(&a.rowkey[lrow], fkey(wm));
       }
     }
-    xsync();  // #1: every CTA's summary is visible to its cluster
+    consumer_sync();
+    const unsigned nf = s_nf;
+    if (!(nf & (kTileOverflow | kTileError))) {
+      const bool in_slot = nf <= unsigned(kSlotCap);
+      float* dv = in_slot ? a.slot_val + tile * kSlotCap : a.pool_val + s_off;
+      int* di = in_slot ? a.slot_idx + tile * kSlotCap : a.pool_idx + s_off;
+      for (unsigned i = tid; i < nf; i += kConsumers) {
+        dv[i] = bval[i];
+        di[i] = bidx[i];
+      }
+    }
+  }
+
+  // Leave only once every stage is idle: a stage whose wait timed out gets one
+  // more bounded wait.
+  for (int sl = 0; sl < kRing; ++sl)
+    if ((lost >> sl) & 1u) (void)mbar_wait(&full[sl], (lost >> (sl + 8)) & 1u);
+}
+
+// ================================================================ finish kernel
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads) sample_finish_kernel(const SampleArgs a) {
+  using E = Elt<DT>;
+  using Sp = Span<DT>;
+  constexpr int EPV = E::kPerVec;
+  constexpr int kLow = int(E::kLowKeyBit);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  extern __shared__ __align__(16) unsigned char fsmem[];
+  float* const bval = reinterpret_cast<float*>(fsmem);         // [kStage]
+  int* const bidx = reinterpret_cast<int*>(bval + kStage);     // [kStage]
+  unsigned* const tstart = reinterpret_cast<unsigned*>(bidx + kStage);  // [kMetaCap + 1]
+  __shared__ Hist hist;  // by radix-pass parity
+  __shared__ float red_f[kWarps], red_s[kWarps], red_b[kWarps];
+  __shared__ int red_i[kWarps], red_n[kWarps], red_bv[kWarps];
+  __shared__ unsigned red_fl[kWarps], red_c[kWarps];
+  __shared__ unsigned scan_c[kWarps];
+  __shared__ unsigned long long scan_m[kWarps];
+  __shared__ int s_sel, s_i[4];
+  __shared__ float s_f[2];
+  __shared__ unsigned s_above_c, s_total, s_nst;
+  __shared__ unsigned long long s_above_m;
+
+  grid_dependency_wait();  // the stream kernel's summaries and buffers are complete
+  // the stream kernel is done with the pool: hand it back empty to the next one
+  if (blockIdx.x == 0 && tid == 0) a.hdr->pool_used = 0u;
+
+  const int lrow = blockIdx.x;
+  const int row = a.row0 + lrow;
+  if (tid == 0) a.rowkey[lrow] = 0u;  // the row's key back to zero for the next call
+  const uint2 key = make_uint2(uint32_t(a.seed), uint32_t(a.seed >> 32));
+  const RowParams rp = row_params(raw_params(a, row));
+  const float T = rp.T, c2 = rp.c2;
+  const bool has_p = rp.has_p, has_m = rp.has_m;
+  const int64_t t0 = int64_t(lrow) * a.tpr;
+  const TileSum* rts = a.ts + t0;
+  const bool meta = a.tpr <= kMetaCap;  // tile starts of the staged buffer fit
+
+  // ------------------------------------------- merge the tile summaries
+  // Thread tid takes a contiguous run of tiles in order, then a fixed tree over
+  // the threads: a deterministic merge.  Buffered entries per tile are counted
+  // for the staging below.
+  {
+    const int per = (a.tpr + kThreads - 1) / kThreads;
+    const int tb = min(tid * per, a.tpr), te = min(tb + per, a.tpr);
+    float wm = -INFINITY, ws = 0.f, wb = -INFINITY;
+    int wv = INT_MAX, wn = 0, wbv = INT_MAX;
+    unsigned flags = 0u, nbuf = 0u;
+    for (int t = tb; t < te; ++t) {
+      const TileSum st = rts[t];
+      wn += st.ncand;
+      row_combine(wm, wv, ws, st.max, st.arg, st.sum, c2, has_p);
+      arg_combine(wb, wbv, st.best, st.best_v);
+      flags |= st.nf & (kTileOverflow | kTileError);
+      const unsigned n = (st.nf & (kTileOverflow | kTileError)) ? 0u : st.nf;
+      if (meta) tstart[t] = n;  // the count, turned into a start below
+      nbuf += n;
+    }
+    // exclusive scan of nbuf over the threads (tile order)
+    unsigned incl = nbuf;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned y = __shfl_up_sync(kFullWarp, incl, o);
+      if (lane >= o) incl += y;
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float m2 = __shfl_xor_sync(kFullWarp, wm, o);
+      const float s2 = __shfl_xor_sync(kFullWarp, ws, o);
+      const int v2 = __shfl_xor_sync(kFullWarp, wv, o);
+      wn += __shfl_xor_sync(kFullWarp, wn, o);
+      row_combine(wm, wv, ws, m2, v2, s2, c2, has_p);
+      const float b2 = __shfl_xor_sync(kFullWarp, wb, o);
+      const int bv2 = __shfl_xor_sync(kFullWarp, wbv, o);
+      arg_combine(wb, wbv, b2, bv2);
+      flags |= __shfl_xor_sync(kFullWarp, flags, o);
+    }
+    if (lane == 31) red_c[warp] = incl;
+    if (lane == 0) {
+      red_f[warp] = wm;
+      red_s[warp] = ws;
+      red_i[warp] = wv;
+      red_n[warp] = wn;
+      red_b[warp] = wb;
+      red_bv[warp] = wbv;
+      red_fl[warp] = flags;
+    }
+    __syncthreads();
+    unsigned base = incl - nbuf;
+    for (int w = 0; w < warp; ++w) base += red_c[w];
+    if (meta) {  // counts -> starts, in place
+      unsigned pos = base;
+      for (int t = tb; t < te; ++t) {
+        const unsigned n = tstart[t];
+        tstart[t] = pos;
+        pos += n;
+      }
+    }
     if (warp == 0) {
-      float wm = -INFINITY, ws = 0.f, wb = -INFINITY;
-      int wv = INT_MAX, wn = 0, wbv = INT_MAX, ov = 0, er = 0;
-      if (lane < C) {
-        const Xchg* p = cluster.map_shared_rank(&xchg[par], lane);
-        wm = p->max;
-        wv = p->arg;
-        ws = p->sum;
-        wn = p->ncand;
-        wb = p->best;
-        wbv = p->best_v;
-        ov = p->overflow;
-        er = p->err;
+      wm = -INFINITY, ws = 0.f, wb = -INFINITY;
+      wv = INT_MAX, wn = 0, wbv = INT_MAX;
+      flags = 0u;
+      unsigned tot = 0u;
+      if (lane < kWarps) {
+        wm = red_f[lane];
+        ws = red_s[lane];
+        wv = red_i[lane];
+        wn = red_n[lane];
+        wb = red_b[lane];
+        wbv = red_bv[lane];
+        flags = red_fl[lane];
+        tot = red_c[lane];
       }
 #pragma unroll
-      for (int o = 16; o; o >>= 1) {
+      for (int o = 4; o; o >>= 1) {
         const float m2 = __shfl_xor_sync(kFullWarp, wm, o);
         const float s2 = __shfl_xor_sync(kFullWarp, ws, o);
         const int v2 = __shfl_xor_sync(kFullWarp, wv, o);
@@ -682,297 +944,336 @@ __global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleArgs a)
         const float b2 = __shfl_xor_sync(kFullWarp, wb, o);
         const int bv2 = __shfl_xor_sync(kFullWarp, wbv, o);
         arg_combine(wb, wbv, b2, bv2);
+        flags |= __shfl_xor_sync(kFullWarp, flags, o);
+        tot += __shfl_xor_sync(kFullWarp, tot, o);
       }
-      ov = __any_sync(kFullWarp, ov != 0);
-      er = __any_sync(kFullWarp, er != 0);
       if (lane == 0) {
         s_f[0] = wm;
         s_f[1] = ws;
         s_i[0] = wv;
         s_i[1] = wn;
         s_i[2] = wbv;
-        s_i[3] = ov | (er << 1);
+        s_i[3] = int(flags >> 30);  // bit 0 overflow, bit 1 error
+        s_total = tot;
+        if (meta) tstart[a.tpr] = tot;
       }
     }
     __syncthreads();
-    const float lmax = s_f[0];
-    const float S = s_f[1];
-    const int larg = s_i[0];
-    const int ncand_ub = s_i[1];  // candidates counted by their bits (-inf included)
-    const bool row_err = (s_i[3] >> 1) != 0;
+  }
+  const float lmax = s_f[0];
+  const float S = s_f[1];
+  const int ncand_ub = s_i[1];  // candidates counted by their bits (-inf included)
+  const bool row_err = (s_i[3] >> 1) != 0;
+  const bool any_overflow = (s_i[3] & 1) != 0;
+  const unsigned total = s_total;
 
-    if (row_err || lmax == -INFINITY || greedy || unfiltered) {
-      if (rank == 0 && tid == 0)
-        a.out[row] = row_err ? -2
-                     : lmax == -INFINITY ? -1
-                     : greedy ? larg
-                              : (s_i[2] == INT_MAX ? -1 : s_i[2]);
-      continue;
-    }
-    const bool any_overflow = (s_i[3] & 1) != 0;
-    const int nbuf = min(s_count, kCap);
-
-    // ------------------------------------------------------- filter bounds
-    if (k > 0 && k >= ncand_ub) k = 0;  // keeps every candidate
-    const bool has_k = k > 0;
-    const float fm = has_m ? fminf(__fadd_ru(lmax, tl), lmax) : -INFINITY;
-    // top-k: the k-th largest per-thread maximum of the cluster bounds t_k from below
-    int jk = -1;
-    if (has_k && !has_m && k <= C * kThreads) {
-      for (int r = 0; r < C; ++r) {
-        const float v = cluster.map_shared_rank(&tmaxs[par][0], r)[tid];
-        if (v > -INFINITY) atomicAdd(&kmerge[kbin(lmax - v)], 1u);
-      }
-      __syncthreads();
-      if (warp == 0) {
-        const unsigned c0 = kmerge[4 * lane], c1 = kmerge[4 * lane + 1];
-        const unsigned cc2 = kmerge[4 * lane + 2], c3 = kmerge[4 * lane + 3];
-        unsigned incl = c0 + c1 + cc2 + c3;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const unsigned y = __shfl_up_sync(kFullWarp, incl, o);
-          if (lane >= o) incl += y;
-        }
-        const unsigned excl = incl - (c0 + c1 + cc2 + c3);
-        const unsigned kk = unsigned(k);
-        int j = -1;
-        if (excl < kk && incl >= kk) {
-          unsigned cum = excl + c0;
-          j = cum >= kk ? 4 * lane
-                        : ((cum += c1) >= kk ? 4 * lane + 1
-                                             : ((cum += cc2) >= kk ? 4 * lane + 2 : 4 * lane + 3));
-        }
-        const unsigned found = __ballot_sync(kFullWarp, j >= 0);
-        j = __shfl_sync(kFullWarp, j, found ? __ffs(found) - 1 : 0);
-        if (lane == 0) s_i[2] = found ? j : -1;
-      }
-      __syncthreads();
-      jk = s_i[2];
-    }
-    float fcut = fm;  // certified lower bound of the keep-threshold
-    if (jk >= 0 && jk < kKBins - 1) fcut = fmaxf(fcut, __fsub_rd(lmax, kbin_hi(jk)));
-    if (has_p) {
-      float D = logf(float(ncand_ub) / (fmaxf(1.f - tp, 1e-30f) * S));
-      D = fmaxf(D, 0.f) * 1.001f + 1e-3f;
-      fcut = fmaxf(fcut, __fsub_rd(lmax, T * D));
-    }
-    // the buffer holds every candidate in [lo_w, lmax]
-    const float lo_w = has_m ? fm : __fsub_ru(lmax, delta);
-
-    // Re-reads this CTA's part from global memory (the ring is prefetching the
-    // next row): f(raw, cb, i0) per vector, warp-uniform.
-    auto reread = [&](auto&& f) {
-      for (int base = 0; base < pt.nvec; base += kThreads) {
-        const int q = base + tid;
-        int i0 = 0;
-        uint32_t cb = 0;
-        uint4 raw = make_uint4(0, 0, 0, 0);
-        if (q < pt.nvec) {
-          cb = pt.bits(q, i0, nullptr, 0, 0);
-          if (cb) raw = pt.gvec(q);
-        }
-        f(raw, cb, i0);
-      }
-    };
-
-    // ---------------------------------- radix select of the threshold
-    unsigned long long P = 0ull;  // fixed-point top-p mass target
-    if (has_p) {
-      const float t = fmaxf(tp, 0.f) * S * 1099511627776.0f;
-      P = t >= 1.8e19f ? ~0ull : static_cast<unsigned long long>(t);
-    }
-    // Largest key x >= key(lo) with count(>= x) >= k (top-k) or mass(>= x) >= P
-    // (top-p), counting candidates of the buffer or of a re-read of the part.
-    // False when none exists.
-    auto descend = [&](bool from_buffer, float lo, uint32_t& out_key) -> bool {
-      const uint32_t klo = fkey(lo), khi = fkey(lmax);
-      const uint32_t diff = klo ^ khi;
-      int top = diff ? 32 - __clz(diff) : kLow + 1;  // one past the highest differing bit
-      top = max(top, kLow + 1);
-      int shift = max(top - 8, kLow);
-      uint32_t prefix = top >= 32 ? 0u : khi & ~((1u << top) - 1u);
-      unsigned above_c = 0;
-      unsigned long long above_m = 0;
-      for (;;) {
-        const int hp = npass & 1;
-        ++npass;
-        hist.cnt[hp][tid] = 0u;
-        hist.mass[hp][tid] = 0ull;
-        if (tid == 0) s_sel = -1;
-        __syncthreads();
-        const uint32_t himask = top >= 32 ? 0u : ~((1u << top) - 1u);
-        const uint32_t dmask = (1u << (top - shift)) - 1u;
-        // warp-uniform: every lane calls with its element (or part = false)
-        auto add = [&](float x, bool part) {
-          int d = -1;
-          if (part && x >= lo) {
-            const uint32_t kx = fkey(x);
-            if (((kx ^ prefix) & himask) == 0u) d = int((kx >> shift) & dmask);
-          }
-          if (!__any_sync(kFullWarp, d >= 0)) return;
-          const unsigned peers = __match_any_sync(kFullWarp, d);
-          if (d < 0) return;
-          const bool leader = lane == __ffs(peers) - 1;
-          if (has_p) {
-            const float e = ex2((x - lmax) * c2);
-            const unsigned long long mm = __float2ull_rn(e * 1099511627776.0f);
-            const unsigned hi = __reduce_add_sync(peers, unsigned(mm >> 20));
-            const unsigned lw = __reduce_add_sync(peers, unsigned(mm & 0xFFFFFu));
-            if (leader)
-              atomicAdd(&hist.mass[hp][d], (static_cast<unsigned long long>(hi) << 20) + lw);
-          }
-          if (leader) atomicAdd(&hist.cnt[hp][d], unsigned(__popc(peers)));
-        };
-        if (from_buffer) {
-          for (int b0 = warp * 32; b0 < nbuf; b0 += kThreads) {
-            const int i = b0 + lane;
-            add(i < nbuf ? bval[i] : 0.f, i < nbuf);
-          }
-        } else {
-          reread([&](const uint4& raw, uint32_t cb, int) {
-            if (!__any_sync(kFullWarp, cb != 0)) return;
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) {
-              const float x = E::get(raw, e);
-              add(x, ((cb >> e) & 1u) && x > -INFINITY);
-            }
-          });
-        }
-        __syncthreads();
-        xsync();
-        // bin tid summed over the cluster, then a descending inclusive scan
-        unsigned c = 0;
-        unsigned long long mass = 0;
-        for (int r = 0; r < C; ++r) {
-          const Hist* h = cluster.map_shared_rank(&hist, r);
-          c += h->cnt[hp][tid];
-          mass += h->mass[hp][tid];
-        }
-        unsigned sc = c;
-        unsigned long long smass = mass;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const unsigned yc = __shfl_down_sync(kFullWarp, sc, o);
-          const unsigned long long ym = __shfl_down_sync(kFullWarp, smass, o);
-          if (lane + o < 32) {
-            sc += yc;
-            smass += ym;
-          }
-        }
-        if (lane == 0) {
-          scan_c[warp] = sc;
-          scan_m[warp] = smass;
-        }
-        __syncthreads();
-        for (int w = warp + 1; w < kWarps; ++w) {
-          sc += scan_c[w];
-          smass += scan_m[w];
-        }
-        const unsigned cc = above_c + sc;
-        const unsigned long long cm = above_m + smass;
-        const bool okb = cc > 0u && ((has_k && cc >= unsigned(k)) || (has_p && cm >= P));
-        if (okb) atomicMax(&s_sel, tid);
-        __syncthreads();
-        const int sel = s_sel;
-        if (sel < 0) return false;
-        if (tid == sel) {
-          s_above_c = cc - c;
-          s_above_m = cm - mass;
-        }
-        __syncthreads();
-        above_c = s_above_c;
-        above_m = s_above_m;
-        prefix |= uint32_t(sel) << shift;
-        if (shift == kLow) {
-          out_key = prefix;
-          return true;
-        }
-        top = shift;
-        shift = max(top - 8, kLow);
-      }
-    };
-
-    float thr = fm;
-    bool from_buffer = !any_overflow;
-    const float lo_b = fmaxf(lo_w, fcut);
-    if (has_k || has_p) {
-      uint32_t kx = 0;
-      bool found = false;
-      if (from_buffer) {
-        found = descend(true, lo_b, kx);
-        if (!found && !(fm >= lo_b)) from_buffer = false;
-      }
-      if (!from_buffer) found = descend(false, fcut, kx);
-      if (found) thr = fmaxf(key_float(kx), fm);
-    } else if (from_buffer && !(fm >= lo_w)) {
-      from_buffer = false;
-    }
-
-    // ----------------------------------------------------------------- draw
-    best = -INFINITY;
-    bestv = INT_MAX;
-    if (from_buffer) {
-      for (int i = tid; i < nbuf; i += kThreads) {
-        const float x = bval[i];
-        if (!(x >= thr)) continue;
-        uint4 w;
-        int g = -1;
-        const int v = bidx[i];
-        arg_combine(best, bestv, score_of(__fdiv_rn(x, T), v, w, g), v);
-      }
-    } else {
-      wgrp = -1;
-      reread([&](const uint4& raw, uint32_t cb, int i0) {
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-          const float x = E::get(raw, e);
-          if (!((cb >> e) & 1u) || !(x >= thr) || !(x > -INFINITY)) continue;
-          const float z = __fdiv_rn(x, T);
-          if (z + kGumbelMax < best) continue;
-          const int v = pt.start + i0 + e;
-          arg_combine(best, bestv, score_of(z, v, w4, wgrp), v);
-        }
-      });
-    }
-    {
-      float wb = best;
-      int wbv = bestv;
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        const float b2 = __shfl_xor_sync(kFullWarp, wb, o);
-        const int bv2 = __shfl_xor_sync(kFullWarp, wbv, o);
-        arg_combine(wb, wbv, b2, bv2);
-      }
-      if (lane == 0) {
-        red_b[warp] = wb;
-        red_bv[warp] = wbv;
-      }
-    }
-    __syncthreads();
-    if (tid == 0) {
-      float wb = -INFINITY;
-      int wbv = INT_MAX;
-      for (int w = 0; w < kWarps; ++w) arg_combine(wb, wbv, red_b[w], red_bv[w]);
-      xchg[par].best = wb;
-      xchg[par].best_v = wbv;
-    }
-    xsync();
-    if (rank == 0 && tid == 0) {
-      float wb = -INFINITY;
-      int wbv = INT_MAX;
-      for (int r = 0; r < C; ++r) {
-        const Xchg* p = cluster.map_shared_rank(&xchg[par], r);
-        arg_combine(wb, wbv, p->best, p->best_v);
-      }
-      a.out[row] = wbv == INT_MAX ? -1 : wbv;
-    }
+  if (row_err || lmax == -INFINITY || rp.greedy || rp.unfiltered) {
+    if (tid == 0)
+      a.out[row] = row_err ? -2
+                   : lmax == -INFINITY ? -1
+                   : rp.greedy ? s_i[0]
+                               : (s_i[2] == INT_MAX ? -1 : s_i[2]);
+    return;
   }
 
-  // Leave only once every stage is idle and the peers are done reading this
-  // CTA: a stage whose wait timed out gets one more bounded wait.
-  for (int sl = 0; sl < kRing; ++sl)
-    if ((lost >> sl) & 1u) (void)mbar_wait(&full[sl], (lost >> (sl + 8)) & 1u);
-  if (C > 1) cluster.sync();
+  // ------------------------------------------------------- filter bounds
+  int k = rp.k;
+  if (k > 0 && k >= ncand_ub) k = 0;  // keeps every candidate
+  const bool has_k = k > 0;
+  const float fm = has_m ? fminf(__fadd_ru(lmax, rp.tl), lmax) : -INFINITY;
+  float fcut = fm;  // certified lower bound of the keep-threshold
+  if (has_p) {
+    float D = logf(float(ncand_ub) / (fmaxf(1.f - rp.tp, 1e-30f) * S));
+    D = fmaxf(D, 0.f) * 1.001f + 1e-3f;
+    fcut = fmaxf(fcut, __fsub_rd(lmax, T * D));
+  }
+  // the tiles' buffers hold every candidate in [lo_w, lmax]
+  const float lo_w = has_m ? fm : __fsub_ru(lmax, rp.delta);
+
+  // ------------------------------- stage the tiles' buffers in shared memory
+  // Entry i of the row (tile order) sits in tile t with tstart[t] <= i <
+  // tstart[t + 1]: independent loads, one per entry.
+  auto fetch = [&](unsigned i, float& x, int& v) {
+    int lo = 0, hi = a.tpr - 1;  // the last tile whose start is <= i
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tstart[mid] <= i)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    const unsigned j = i - tstart[lo];
+    if (tstart[lo + 1] - tstart[lo] <= unsigned(kSlotCap)) {
+      x = a.slot_val[(t0 + lo) * kSlotCap + j];
+      v = a.slot_idx[(t0 + lo) * kSlotCap + j];
+    } else {
+      const unsigned off = rts[lo].off;
+      x = a.pool_val[off + j];
+      v = a.pool_idx[off + j];
+    }
+  };
+  const bool flat = meta && !any_overflow;  // entries addressable by their row position
+  const float lo_b = fmaxf(lo_w, fcut);      // nothing below can be kept
+  // Stage the entries at or above lo_b (the only ones any pass counts) in
+  // shared memory; when they do not fit, every pass reads the workspace.
+  unsigned nst = 0;
+  bool staged = false;
+  if (flat) {
+    if (tid == 0) s_nst = 0u;
+    __syncthreads();
+    for (unsigned b0 = unsigned(warp) * 32u; b0 < total; b0 += kThreads) {
+      const unsigned i = b0 + lane;
+      float x = 0.f;
+      int v = 0;
+      bool keep = false;
+      if (i < total) {
+        fetch(i, x, v);
+        keep = x >= lo_b;
+      }
+      const unsigned bal = __ballot_sync(kFullWarp, keep);
+      unsigned base = 0u;
+      if (lane == 0 && bal) base = atomicAdd(&s_nst, unsigned(__popc(bal)));
+      base = __shfl_sync(kFullWarp, base, 0);
+      if (keep) {
+        const unsigned pos = base + unsigned(__popc(bal & ((1u << lane) - 1u)));
+        if (pos < unsigned(kStage)) {
+          bval[pos] = x;
+          bidx[pos] = v;
+        }
+      }
+    }
+    __syncthreads();
+    nst = s_nst;
+    staged = nst <= unsigned(kStage);
+  }
+
+  // The row's buffered entries: f(x, token, valid), warp-uniform; the staged
+  // ones from shared memory, else all of them from the workspace.
+  auto buffered = [&](auto&& f) {
+    if (staged) {
+      for (unsigned b0 = unsigned(warp) * 32u; b0 < nst; b0 += kThreads) {
+        const unsigned i = b0 + lane;
+        const bool ok = i < nst;
+        f(ok ? bval[i] : 0.f, ok ? bidx[i] : 0, ok);
+      }
+      return;
+    }
+    if (flat) {
+      for (unsigned b0 = unsigned(warp) * 32u; b0 < total; b0 += kThreads) {
+        const unsigned i = b0 + lane;
+        const bool ok = i < total;
+        float x = 0.f;
+        int v = 0;
+        if (ok) fetch(i, x, v);
+        f(x, v, ok);
+      }
+      return;
+    }
+    for (int t = 0; t < a.tpr; ++t) {
+      const unsigned n = rts[t].nf;
+      if (n & (kTileOverflow | kTileError)) continue;
+      const bool in_slot = n <= unsigned(kSlotCap);
+      const float* sv = in_slot ? a.slot_val + (t0 + t) * kSlotCap : a.pool_val + rts[t].off;
+      const int* si = in_slot ? a.slot_idx + (t0 + t) * kSlotCap : a.pool_idx + rts[t].off;
+      for (unsigned b0 = unsigned(warp) * 32u; b0 < n; b0 += kThreads) {
+        const unsigned i = b0 + lane;
+        const bool ok = i < n;
+        f(ok ? sv[i] : 0.f, ok ? si[i] : 0, ok);
+      }
+    }
+  };
+  // Re-reads the whole row from global memory: f(raw, cb, i0) per vector,
+  // warp-uniform.
+  Sp rw;
+  bool rw_ready = false;
+  auto reread = [&](auto&& f) {
+    if (!rw_ready) {
+      rw.init(a, row, 0, a.V, row_masked(a, row));
+      rw_ready = true;
+    }
+    for (int base = 0; base < rw.nvec; base += kThreads) {
+      const int q = base + tid;
+      int i0 = 0;
+      uint32_t cb = 0;
+      uint4 raw = make_uint4(0, 0, 0, 0);
+      if (q < rw.nvec) {
+        cb = rw.bits(q, i0, nullptr, 0, 0);
+        if (cb) raw = rw.gvec(q);
+      }
+      f(raw, cb, i0);
+    }
+  };
+
+  // ---------------------------------- radix select of the threshold
+  unsigned long long P = 0ull;  // fixed-point top-p mass target
+  if (has_p) {
+    const float t = fmaxf(rp.tp, 0.f) * S * 1099511627776.0f;
+    P = t >= 1.8e19f ? ~0ull : static_cast<unsigned long long>(t);
+  }
+  int npass = 0;  // histogram parity
+  // Largest key x >= key(lo) with count(>= x) >= k (top-k) or mass(>= x) >= P
+  // (top-p), counting candidates of the tiles' buffers or of a re-read of the
+  // row.  False when none exists.
+  auto descend = [&](bool from_buffers, float lo, uint32_t& out_key) -> bool {
+    const uint32_t klo = fkey(lo), khi = fkey(lmax);
+    const uint32_t diff = klo ^ khi;
+    int top = diff ? 32 - __clz(diff) : kLow + 1;  // one past the highest differing bit
+    top = max(top, kLow + 1);
+    int shift = max(top - 8, kLow);
+    uint32_t prefix = top >= 32 ? 0u : khi & ~((1u << top) - 1u);
+    unsigned above_c = 0;
+    unsigned long long above_m = 0;
+    for (;;) {
+      const int hp = npass & 1;
+      ++npass;
+      hist.cnt[hp][tid] = 0u;
+      hist.mass[hp][tid] = 0ull;
+      if (tid == 0) s_sel = -1;
+      __syncthreads();
+      const uint32_t himask = top >= 32 ? 0u : ~((1u << top) - 1u);
+      const uint32_t dmask = (1u << (top - shift)) - 1u;
+      // warp-uniform: every lane calls with its element (or part = false)
+      auto add = [&](float x, bool part) {
+        int d = -1;
+        if (part && x >= lo) {
+          const uint32_t kx = fkey(x);
+          if (((kx ^ prefix) & himask) == 0u) d = int((kx >> shift) & dmask);
+        }
+        if (!__any_sync(kFullWarp, d >= 0)) return;
+        const unsigned peers = __match_any_sync(kFullWarp, d);
+        if (d < 0) return;
+        const bool leader = lane == __ffs(peers) - 1;
+        if (has_p) {
+          const float e = ex2((x - lmax) * c2);
+          const unsigned long long mm = __float2ull_rn(e * 1099511627776.0f);
+          const unsigned hi = __reduce_add_sync(peers, unsigned(mm >> 20));
+          const unsigned lw = __reduce_add_sync(peers, unsigned(mm & 0xFFFFFu));
+          if (leader)
+            atomicAdd(&hist.mass[hp][d], (static_cast<unsigned long long>(hi) << 20) + lw);
+        }
+        if (leader) atomicAdd(&hist.cnt[hp][d], unsigned(__popc(peers)));
+      };
+      if (from_buffers) {
+        buffered([&](float x, int, bool ok) { add(x, ok); });
+      } else {
+        reread([&](const uint4& raw, uint32_t cb, int) {
+          if (!__any_sync(kFullWarp, cb != 0)) return;
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) {
+            const float x = E::get(raw, e);
+            add(x, ((cb >> e) & 1u) && x > -INFINITY);
+          }
+        });
+      }
+      __syncthreads();
+      // bin tid, then a descending inclusive scan over the bins
+      const unsigned c = hist.cnt[hp][tid];
+      const unsigned long long mass = hist.mass[hp][tid];
+      unsigned sc = c;
+      unsigned long long smass = mass;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned yc = __shfl_down_sync(kFullWarp, sc, o);
+        const unsigned long long ym = __shfl_down_sync(kFullWarp, smass, o);
+        if (lane + o < 32) {
+          sc += yc;
+          smass += ym;
+        }
+      }
+      if (lane == 0) {
+        scan_c[warp] = sc;
+        scan_m[warp] = smass;
+      }
+      __syncthreads();
+      for (int w = warp + 1; w < kWarps; ++w) {
+        sc += scan_c[w];
+        smass += scan_m[w];
+      }
+      const unsigned cc = above_c + sc;
+      const unsigned long long cm = above_m + smass;
+      const bool okb = cc > 0u && ((has_k && cc >= unsigned(k)) || (has_p && cm >= P));
+      if (okb) atomicMax(&s_sel, tid);
+      __syncthreads();
+      const int sel = s_sel;
+      if (sel < 0) return false;
+      if (tid == sel) {
+        s_above_c = cc - c;
+        s_above_m = cm - mass;
+      }
+      __syncthreads();
+      above_c = s_above_c;
+      above_m = s_above_m;
+      prefix |= uint32_t(sel) << shift;
+      if (shift == kLow) {
+        out_key = prefix;
+        return true;
+      }
+      top = shift;
+      shift = max(top - 8, kLow);
+    }
+  };
+
+  float thr = fm;
+  bool from_buffers = !any_overflow;
+  if (has_k || has_p) {
+    uint32_t kx = 0;
+    bool found = false;
+    if (from_buffers) {
+      found = descend(true, lo_b, kx);
+      if (!found && !(fm >= lo_b)) from_buffers = false;
+    }
+    if (!from_buffers) found = descend(false, fcut, kx);
+    if (found) thr = fmaxf(key_float(kx), fm);
+  } else if (from_buffers && !(fm >= lo_w)) {
+    from_buffers = false;
+  }
+
+  // ----------------------------------------------------------------- draw
+  float best = -INFINITY;
+  int bestv = INT_MAX;
+  if (from_buffers) {
+    buffered([&](float x, int v, bool ok) {
+      if (!ok || !(x >= thr)) return;
+      uint4 w;
+      int g = -1;
+      arg_combine(best, bestv, gumbel_score(__fdiv_rn(x, T), v, row, a.offset, key, w, g), v);
+    });
+  } else {
+    uint4 w4 = make_uint4(0, 0, 0, 0);
+    int wgrp = -1;
+    reread([&](const uint4& raw, uint32_t cb, int i0) {
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        const float x = E::get(raw, e);
+        if (!((cb >> e) & 1u) || !(x >= thr) || !(x > -INFINITY)) continue;
+        const float z = __fdiv_rn(x, T);
+        if (z + kGumbelMax < best) continue;
+        const int v = rw.start + i0 + e;
+        arg_combine(best, bestv, gumbel_score(z, v, row, a.offset, key, w4, wgrp), v);
+      }
+    });
+  }
+  {
+    float wb = best;
+    int wbv = bestv;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float b2 = __shfl_xor_sync(kFullWarp, wb, o);
+      const int bv2 = __shfl_xor_sync(kFullWarp, wbv, o);
+      arg_combine(wb, wbv, b2, bv2);
+    }
+    if (lane == 0) {
+      red_b[warp] = wb;
+      red_bv[warp] = wbv;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float wb = -INFINITY;
+    int wbv = INT_MAX;
+    for (int w = 0; w < kWarps; ++w) arg_combine(wb, wbv, red_b[w], red_bv[w]);
+    a.out[row] = wbv == INT_MAX ? -1 : wbv;
+  }
 }
 
 __global__ void philox_kernel(const uint32_t* __restrict__ ctr, const uint32_t* __restrict__ key,
@@ -991,7 +1292,6 @@ __global__ void philox_kernel(const uint32_t* __restrict__ ctr, const uint32_t* 
 
 // ------------------------------------------------------------------- host
 
-
 int num_sms() {
   static int n = [] {
     int dev = 0, v = 148;
@@ -1002,99 +1302,139 @@ int num_sms() {
   return n;
 }
 
-// Tokens per CTA when a row is split over S CTAs (a multiple of 32, so a CTA's
-// bitmask words are its own).
-int64_t chunk_for(int64_t V, int S) {
-  int64_t c = (V + S - 1) / S;
-  c = (c + 31) / 32 * 32;
-  return std::max<int64_t>(c, 32);
+int elt_bytes(lp_dtype dt) { return dt == LP_F32 ? 4 : 2; }
+
+// Tokens per tile for a launch of nrows rows: the longest tile that still
+// gives kTileTarget tiles (enough for every CTA of the grid to take two), down
+// to the shortest.  It does not depend on the device, so the workspace size can
+// follow it exactly.
+int64_t tile_tokens(int eb, int64_t nrows, int64_t V) {
+  int64_t tile = kTileBytesMax / eb;
+  while (tile > kTileBytesMin / eb && nrows * std::max<int64_t>(1, (V + tile - 1) / tile) <
+                                          kTileTarget)
+    tile /= 2;
+  return tile;
+}
+int64_t tiles_per_row(int64_t tile, int64_t V) {
+  return std::max<int64_t>(1, (V + tile - 1) / tile);
 }
 
-// CTAs per row: one, unless there are fewer rows than SMs; then rows are split
-// over clusters until every SM has work, keeping at least 4096 tokens per CTA.
-int split_for(int64_t B, int64_t V) {
-  int S = 1;
-  while (S < kMaxSplit && B * S < int64_t(num_sms()) && chunk_for(V, 2 * S) >= 4096) S *= 2;
-  return S;
+// Workspace layout for a call of B rows of V tokens: rows per launch, tiles per
+// launch at most, and the offsets of the tile summaries, the tiles' slots and
+// the pool.
+struct WsPlan {
+  int64_t rows, tiles, pool;
+  int64_t ts_off, sv_off, si_off, pv_off, pi_off, bytes;
+};
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+WsPlan ws_plan(lp_dtype dt, int64_t B, int64_t V) {
+  WsPlan p{};
+  const int eb = elt_bytes(dt);
+  const int64_t tpr_max = tiles_per_row(kTileBytesMin / eb, V);
+  p.rows = std::max<int64_t>(1, std::min({B, kMaxRowsPerLaunch, kMaxTileSums / tpr_max}));
+  // full launches, and the last, shorter one (whose tiles may be shorter)
+  p.tiles = p.rows * tiles_per_row(tile_tokens(eb, p.rows, V), V);
+  const int64_t last = B % p.rows;
+  if (last) p.tiles = std::max(p.tiles, last * tiles_per_row(tile_tokens(eb, last, V), V));
+  p.pool = std::min(std::max(p.rows * kPoolPerRow, kPoolMin), kPoolMax);
+  // The header and the per-row keys must be zero when a call starts; they sit
+  // in a region of fixed size at the front, which no call of any shape uses for
+  // anything else, and every call leaves them zero.
+  p.ts_off = int64_t(sizeof(WsHeader)) + 4 * kMaxRowsPerLaunch;
+  p.sv_off = round_up(p.ts_off + p.tiles * int64_t(sizeof(TileSum)), 256);
+  p.si_off = round_up(p.sv_off + p.tiles * kSlotCap * 4, 256);
+  p.pv_off = round_up(p.si_off + p.tiles * kSlotCap * 4, 256);
+  p.pi_off = round_up(p.pv_off + p.pool * 4, 256);
+  p.bytes = round_up(p.pi_off + p.pool * 4, 256);
+  return p;
 }
 
 template <int DT>
-cudaError_t launch_sample(SampleArgs a, int64_t B, int64_t V, cudaStream_t s) {
+int resident_ctas() {
+  static int n = [] {
+    int per_sm = 0;
+    if (cudaFuncSetAttribute(sample_stream_kernel<DT>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sample_stream_kernel<DT>, kThreads,
+                                                      size_t(kSmem)) != cudaSuccess ||
+        cudaFuncSetAttribute(sample_finish_kernel<DT>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kFinishSmem) != cudaSuccess ||
+        per_sm <= 0) {
+      (void)cudaGetLastError();
+      per_sm = 1;
+    }
+    return per_sm * num_sms();
+  }();
+  return n;
+}
+
+template <int DT>
+cudaError_t launch_sample(SampleArgs a, const WsPlan& plan, int64_t B, char* ws,
+                          cudaStream_t s) {
   static std::mutex mu;
-  static bool configured = false;
-  static std::map<int, int> clusters;  // resident clusters by cluster size
-  int S = split_for(B, V);
-  int resident = 0;
+  int G;
   {
     std::lock_guard<std::mutex> lock(mu);
-    if (!configured) {
-      cudaError_t e = cudaFuncSetAttribute(sample_kernel<DT>,
-                                           cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-      if (e != cudaSuccess) return e;
-      e = cudaFuncSetAttribute(sample_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSmem);
-      if (e != cudaSuccess) return e;
-      configured = true;
-    }
-    for (;;) {
-      auto it = clusters.find(S);
-      if (it == clusters.end()) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(unsigned(S) * 64u);
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = size_t(kSmem);
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = unsigned(S);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, sample_kernel<DT>, &cfg) != cudaSuccess) {
-          (void)cudaGetLastError();
-          n = 0;
-        }
-        it = clusters.emplace(S, n).first;
-      }
-      resident = it->second;
-      if (resident > 0 || S == 1) break;
-      S /= 2;  // this cluster shape cannot be co-scheduled: try a smaller one
-    }
+    G = resident_ctas<DT>();
   }
-  if (resident <= 0) resident = std::max(1, 3 * num_sms() / S);
-  a.chunk = int(chunk_for(V, S));
-  a.ncl = int(std::min<int64_t>(B, resident));
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(a.ncl) * unsigned(S));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = size_t(kSmem);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = unsigned(S);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, sample_kernel<DT>, a);
+  const int eb = DT == LP_F32 ? 4 : 2;
+  a.hdr = reinterpret_cast<WsHeader*>(ws);
+  a.rowkey = reinterpret_cast<unsigned*>(ws + sizeof(WsHeader));
+  a.ts = reinterpret_cast<TileSum*>(ws + plan.ts_off);
+  a.slot_val = reinterpret_cast<float*>(ws + plan.sv_off);
+  a.slot_idx = reinterpret_cast<int*>(ws + plan.si_off);
+  a.pool_val = reinterpret_cast<float*>(ws + plan.pv_off);
+  a.pool_idx = reinterpret_cast<int*>(ws + plan.pi_off);
+  a.pool_cap = unsigned(plan.pool);
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  for (int64_t r0 = 0; r0 < B; r0 += plan.rows) {
+    const int64_t nr = std::min(plan.rows, B - r0);
+    const int64_t tile = tile_tokens(eb, nr, a.V);
+    a.row0 = int(r0);
+    a.nrows = int(nr);
+    a.chunk = int(tile);
+    a.tpr = int(tiles_per_row(tile, a.V));
+    a.ntiles = nr * a.tpr;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(std::min<int64_t>(a.ntiles, G)));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = size_t(kSmem);
+    cfg.stream = s;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, sample_stream_kernel<DT>, a);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(unsigned(nr));
+    cfg.dynamicSmemBytes = size_t(kFinishSmem);
+    e = cudaLaunchKernelEx(&cfg, sample_finish_kernel<DT>, a);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 lp_status run_sample(const void* logits, lp_dtype dt, int64_t B, int64_t vocab,
                      int64_t logits_stride, const int32_t* bitmask, int64_t bitmask_rows,
                      int64_t bitmask_stride, const int32_t* indices, int64_t num_indices,
-                     const lp_sampling_params* params, int64_t* out_ids, cudaStream_t stream) {
+                     const lp_sampling_params* params, int64_t* out_ids, void* workspace,
+                     int64_t workspace_bytes, cudaStream_t stream) {
   if (B == 0) return LP_OK;
   if (logits == nullptr && vocab > 0) return LP_ERR_INVALID_ARGUMENT;
   if (out_ids == nullptr || params == nullptr) return LP_ERR_INVALID_ARGUMENT;
-  if (B * int64_t(kMaxSplit) > 0x7fffffff || vocab > 0x7fffffff - 64 ||
-      num_indices > 0x7fffffff)
+  if (B > (int64_t(1) << 27) || vocab > 0x7fffffff - 64 || num_indices > 0x7fffffff)
     return LP_ERR_TOO_LARGE;
-  const int eb = dt == LP_F32 ? 4 : 2;
+  const WsPlan plan = ws_plan(dt, B, vocab);
+  if (workspace == nullptr || workspace_bytes < plan.bytes ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+    return LP_ERR_INVALID_ARGUMENT;
+  const int eb = elt_bytes(dt);
   SampleArgs a{};
   a.logits = static_cast<const char*>(logits);
   a.stride_bytes = logits_stride * eb;
-  a.B = int(B);
   a.V = int(vocab);
   a.bitmask = reinterpret_cast<const uint32_t*>(bitmask);
   a.bm_stride = bitmask_stride;
@@ -1112,11 +1452,12 @@ lp_status run_sample(const void* logits, lp_dtype dt, int64_t B, int64_t vocab,
   a.seed = params->seed;
   a.offset = params->offset;
   a.out = out_ids;
+  char* ws = static_cast<char*>(workspace);
   cudaError_t e;
   switch (dt) {
-    case LP_F32: e = launch_sample<LP_F32>(a, B, vocab, stream); break;
-    case LP_F16: e = launch_sample<LP_F16>(a, B, vocab, stream); break;
-    default: e = launch_sample<LP_BF16>(a, B, vocab, stream); break;
+    case LP_F32: e = launch_sample<LP_F32>(a, plan, B, ws, stream); break;
+    case LP_F16: e = launch_sample<LP_F16>(a, plan, B, ws, stream); break;
+    default: e = launch_sample<LP_BF16>(a, plan, B, ws, stream); break;
   }
   return e == cudaSuccess ? LP_OK : LP_ERR_CUDA;
 }
@@ -1126,13 +1467,20 @@ lp_status run_sample(const void* logits, lp_dtype dt, int64_t B, int64_t vocab,
 
 using namespace lp;
 
+extern "C" int64_t lp_sample_workspace_bytes(lp_dtype dt, int64_t B, int64_t vocab_size) {
+  if (!(dt == LP_F32 || dt == LP_F16 || dt == LP_BF16) || B < 0 || vocab_size < 0) return -1;
+  if (B == 0) return 0;
+  return ws_plan(dt, B, vocab_size).bytes;
+}
+
 extern "C" lp_status lp_sample(const void* logits, lp_dtype dt, int64_t B, int64_t vocab_size,
                                int64_t logits_stride, const lp_sampling_params* params,
-                               int64_t* out_ids, cudaStream_t stream) {
+                               int64_t* out_ids, void* workspace, int64_t workspace_bytes,
+                               cudaStream_t stream) {
   if (!(dt == LP_F32 || dt == LP_F16 || dt == LP_BF16)) return LP_ERR_UNSUPPORTED_DTYPE;
   if (B < 0 || vocab_size < 0 || logits_stride < vocab_size) return LP_ERR_INVALID_ARGUMENT;
   return run_sample(logits, dt, B, vocab_size, logits_stride, nullptr, 0, 0, nullptr, 0, params,
-                    out_ids, stream);
+                    out_ids, workspace, workspace_bytes, stream);
 }
 
 extern "C" lp_status lp_mask_and_sample(const void* logits, lp_dtype dt, int64_t B, int64_t cols,
@@ -1141,6 +1489,7 @@ extern "C" lp_status lp_mask_and_sample(const void* logits, lp_dtype dt, int64_t
                                         int64_t bitmask_stride, int64_t vocab_size,
                                         const int32_t* indices, int64_t num_indices,
                                         const lp_sampling_params* params, int64_t* out_ids,
+                                        void* workspace, int64_t workspace_bytes,
                                         cudaStream_t stream) {
   if (!(dt == LP_F32 || dt == LP_F16 || dt == LP_BF16)) return LP_ERR_UNSUPPORTED_DTYPE;
   if (B < 0 || cols < 0 || logits_stride < cols || num_indices < 0 ||
@@ -1150,7 +1499,7 @@ extern "C" lp_status lp_mask_and_sample(const void* logits, lp_dtype dt, int64_t
     const int64_t vocab = vocab_size < 0 ? cols : vocab_size;
     if (vocab > cols) return LP_ERR_INVALID_ARGUMENT;
     return run_sample(logits, dt, B, vocab, logits_stride, nullptr, 0, 0, nullptr, 0, params,
-                      out_ids, stream);
+                      out_ids, workspace, workspace_bytes, stream);
   }
   if (bitmask_words < 0 || bitmask_stride < bitmask_words || bitmask_rows < 0)
     return LP_ERR_INVALID_ARGUMENT;
@@ -1160,7 +1509,8 @@ extern "C" lp_status lp_mask_and_sample(const void* logits, lp_dtype dt, int64_t
   if (indices == nullptr && bitmask_rows < B) return LP_ERR_INVALID_ARGUMENT;
   const bool any_masked = indices == nullptr || num_indices > 0;
   return run_sample(logits, dt, B, vocab, logits_stride, any_masked ? bitmask : nullptr,
-                    bitmask_rows, bitmask_stride, indices, num_indices, params, out_ids, stream);
+                    bitmask_rows, bitmask_stride, indices, num_indices, params, out_ids,
+                    workspace, workspace_bytes, stream);
 }
 
 extern "C" lp_status lp_philox4x32_10(const uint32_t* counters, const uint32_t* keys,
@@ -1179,7 +1529,7 @@ extern "C" const char* lp_status_string(lp_status status) {
     case LP_ERR_INVALID_ARGUMENT: return "invalid argument";
     case LP_ERR_UNSUPPORTED_DTYPE: return "unsupported dtype";
     case LP_ERR_CUDA: return "CUDA launch failed";
-    case LP_ERR_TOO_LARGE: return "row too long for the sampler";
+    case LP_ERR_TOO_LARGE: return "size past the kernels' 32-bit index range";
     default: return "unknown status";
   }
 }

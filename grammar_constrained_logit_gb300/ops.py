@@ -160,21 +160,51 @@ def _ids_out(out, B, device):
     return out
 
 
+_workspaces: dict = {}
+
+
+def sample_workspace_bytes(dtype: torch.dtype, batch_size: int, vocab_size: int) -> int:
+    """Bytes of device scratch ``sample`` / ``mask_and_sample`` need."""
+    n = _lib.load().lp_sample_workspace_bytes(_DT[dtype], batch_size, vocab_size)
+    if n < 0:
+        raise ValueError("invalid dtype or size")
+    return int(n)
+
+
+def _workspace(workspace, lg: torch.Tensor, B: int, vocab: int):
+    """The caller's workspace (a zero-filled uint8 CUDA tensor), or one kept per
+    (device, stream), grown on demand.  The library leaves it zero-filled after
+    every call.  Returns (pointer, bytes)."""
+    need = sample_workspace_bytes(lg.dtype, B, max(vocab, 0))
+    if workspace is not None:
+        if workspace.dtype != torch.uint8 or not workspace.is_contiguous() or \
+                workspace.device != lg.device:
+            raise ValueError("workspace must be a contiguous uint8 tensor on the logits' device")
+        return ctypes.c_void_p(workspace.data_ptr()), workspace.numel()
+    key = (lg.device.index, torch.cuda.current_stream(lg.device).cuda_stream)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros(max(need, 1), dtype=torch.uint8, device=lg.device)
+        _workspaces[key] = ws
+    return ctypes.c_void_p(ws.data_ptr()), ws.numel()
+
+
 def sample(logits: torch.Tensor, temperature=1.0, top_k=0, top_p=1.0, min_p=0.0, seed: int = 0,
            offset: int = 0, *, vocab_size: int | None = None,
-           out: torch.Tensor | None = None) -> torch.Tensor:
+           out: torch.Tensor | None = None, workspace: torch.Tensor | None = None) -> torch.Tensor:
     """Temperature, top-k ∩ top-p ∩ min-p, Gumbel-max draw keyed by
     (seed, row, offset); greedy for temperature <= 0 or top_k == 1.  Every
     parameter is a scalar or a length-B tensor.  Returns int64 ids [B]."""
     lg = _matrix(logits, "logits")
     B = lg.size(0)
+    V = lg.size(1) if vocab_size is None else int(vocab_size)
     keep: list = []
     p = _params(B, lg.device, temperature, top_k, top_p, min_p, seed, offset, keep)
     ids = _ids_out(out, B, lg.device)
+    wp, wn = _workspace(workspace, lg, B, V)
     lib = _lib.load()
-    st = lib.lp_sample(_ptr(lg), _dtype_code(lg), B,
-                       lg.size(1) if vocab_size is None else int(vocab_size), _stride(lg),
-                       ctypes.byref(p), _ptr(ids), _stream(lg))
+    st = lib.lp_sample(_ptr(lg), _dtype_code(lg), B, V, _stride(lg),
+                       ctypes.byref(p), _ptr(ids), wp, wn, _stream(lg))
     check("lp_sample", st)
     return ids
 
@@ -186,7 +216,8 @@ def mask_and_sample(logits: torch.Tensor, bitmask: torch.Tensor | None, temperat
                     top_k=0, top_p=1.0, min_p=0.0, seed: int = 0, offset: int = 0, *,
                     indices: Sequence[int] | torch.Tensor | None = None,
                     vocab_size: int | None = None,
-                    out: torch.Tensor | None = None) -> torch.Tensor:
+                    out: torch.Tensor | None = None,
+                    workspace: torch.Tensor | None = None) -> torch.Tensor:
     """The bitmask applied on the fly (logits are not written), then ``sample``.
     Rows in ``indices`` (all rows when None) are masked; a masked row whose mask
     admits no token returns -1."""
@@ -197,12 +228,15 @@ def mask_and_sample(logits: torch.Tensor, bitmask: torch.Tensor | None, temperat
     keep: list = []
     p = _params(B, lg.device, temperature, top_k, top_p, min_p, seed, offset, keep)
     ids = _ids_out(out, B, lg.device)
+    # the workspace is sized by the widest vocabulary the call can use
+    wp, wn = _workspace(workspace, lg, B, lg.size(1))
     lib = _lib.load()
     st = lib.lp_mask_and_sample(
         _ptr(lg), _dtype_code(lg), B, lg.size(1), _stride(lg), _ptr(bm),
         0 if bm is None else bm.size(0), 0 if bm is None else bm.size(1),
         0 if bm is None else _stride(bm), -1 if vocab_size is None else int(vocab_size),
-        _ptr(idx), 0 if idx is None else idx.numel(), ctypes.byref(p), _ptr(ids), _stream(lg))
+        _ptr(idx), 0 if idx is None else idx.numel(), ctypes.byref(p), _ptr(ids), wp, wn,
+        _stream(lg))
     check("lp_mask_and_sample", st)
     return ids
 

@@ -135,13 +135,35 @@ lp_status lp_apply_packed_bitmask(void* out, int64_t out_stride, const void* log
  *   hi32(offset)) and key (lo32(seed), hi32(seed)).
  *   out_ids        device int64 [B]
  *   params         host pointer, see lp_sampling_params
+ *   workspace      device scratch of at least lp_sample_workspace_bytes(dt, B,
+ *                  vocab_size) bytes, 256-byte aligned, owned by the caller.  It
+ *                  must be zero-filled before its first use; after that the
+ *                  library keeps it valid itself (every call leaves the counters
+ *                  at its front zero), so one allocation serves any number of
+ *                  calls of the same or smaller size.  Calls that share a workspace must
+ *                  be ordered (one stream, or events).  A NULL, misaligned or
+ *                  short workspace is LP_ERR_INVALID_ARGUMENT.
+ * Each call is two kernels on the stream: a streaming pass over the logits and
+ * a per-row finish, the second launched as a programmatic dependent of the
+ * first.  An id of -2 means a copy into shared memory did not complete within
+ * the kernel's bounded wait (no such case is known).
  * Logits are read only.  vocab_size up to 2^31 - 65 and B up to 2^27 are
  * supported; larger sizes return LP_ERR_TOO_LARGE.
  */
 
+/*
+ * lp_sample_workspace_bytes -- bytes of device scratch lp_sample and
+ * lp_mask_and_sample need for B rows of vocab_size tokens of type dt: per-tile
+ * summaries and candidate slots plus a pool for longer candidate buffers --
+ * at most about 7% of the logits' size plus 128 MB.  0 for B == 0; -1 for an
+ * invalid dt or a negative size.  The result does not depend on the device.
+ */
+int64_t lp_sample_workspace_bytes(lp_dtype dt, int64_t B, int64_t vocab_size);
+
 lp_status lp_sample(const void* logits, lp_dtype dt, int64_t B, int64_t vocab_size,
                     int64_t logits_stride, const lp_sampling_params* params,
-                    int64_t* out_ids, cudaStream_t stream);
+                    int64_t* out_ids, void* workspace, int64_t workspace_bytes,
+                    cudaStream_t stream);
 
 /*
  * lp_mask_and_sample -- the bitmask of lp_apply_token_bitmask applied on the fly
@@ -158,7 +180,7 @@ lp_status lp_mask_and_sample(const void* logits, lp_dtype dt, int64_t B, int64_t
                              int64_t bitmask_stride, int64_t vocab_size,
                              const int32_t* indices, int64_t num_indices,
                              const lp_sampling_params* params, int64_t* out_ids,
-                             cudaStream_t stream);
+                             void* workspace, int64_t workspace_bytes, cudaStream_t stream);
 
 /*
  * lp_philox4x32_10 -- diagnostic: the device's Philox4x32-10 (Salmon et al.,

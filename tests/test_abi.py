@@ -108,25 +108,49 @@ def _params():
     return p
 
 
+WS = ctypes.c_void_p(0x100000)  # 256-byte aligned; never dereferenced
+WSN = 1 << 40
+
+
 def test_sample_validation(lib):
     p = _params()
     out = ctypes.c_void_p(0x3000)
-    assert lib.lp_sample(FAKE, 0, -1, 10, 10, ctypes.byref(p), out, None) == \
-        _lib.LP_ERR_INVALID_ARGUMENT
-    assert lib.lp_sample(FAKE, 0, 2, 10, 9, ctypes.byref(p), out, None) == \
-        _lib.LP_ERR_INVALID_ARGUMENT
-    assert lib.lp_sample(FAKE, 5, 2, 10, 10, ctypes.byref(p), out, None) == \
-        _lib.LP_ERR_UNSUPPORTED_DTYPE
-    assert lib.lp_sample(FAKE, 0, 2, 10, 10, None, out, None) == _lib.LP_ERR_INVALID_ARGUMENT
-    assert lib.lp_sample(FAKE, 0, 2, 10, 10, ctypes.byref(p), None, None) == \
-        _lib.LP_ERR_INVALID_ARGUMENT
-    assert lib.lp_sample(None, 0, 0, 10, 10, ctypes.byref(p), None, None) == _lib.LP_OK
+    call = lambda logits, dt, B, V, stride, params, o, ws=WS, wsn=WSN: lib.lp_sample(  # noqa: E731
+        logits, dt, B, V, stride, params, o, ws, wsn, None)
+    assert call(FAKE, 0, -1, 10, 10, ctypes.byref(p), out) == _lib.LP_ERR_INVALID_ARGUMENT
+    assert call(FAKE, 0, 2, 10, 9, ctypes.byref(p), out) == _lib.LP_ERR_INVALID_ARGUMENT
+    assert call(FAKE, 5, 2, 10, 10, ctypes.byref(p), out) == _lib.LP_ERR_UNSUPPORTED_DTYPE
+    assert call(FAKE, 0, 2, 10, 10, None, out) == _lib.LP_ERR_INVALID_ARGUMENT
+    assert call(FAKE, 0, 2, 10, 10, ctypes.byref(p), None) == _lib.LP_ERR_INVALID_ARGUMENT
+    assert call(None, 0, 0, 10, 10, ctypes.byref(p), None, None, 0) == _lib.LP_OK
     # sizes past the kernels' 32-bit index range are refused before any launch
     huge = 2**31
-    assert lib.lp_sample(FAKE, 1, 2, huge, huge, ctypes.byref(p), out, None) == \
-        _lib.LP_ERR_TOO_LARGE
-    assert lib.lp_sample(FAKE, 1, 2**28, 8, 8, ctypes.byref(p), out, None) == \
-        _lib.LP_ERR_TOO_LARGE
+    assert call(FAKE, 1, 2, huge, huge, ctypes.byref(p), out) == _lib.LP_ERR_TOO_LARGE
+    assert call(FAKE, 1, 2**28, 8, 8, ctypes.byref(p), out) == _lib.LP_ERR_TOO_LARGE
+    # the workspace: present, 256-byte aligned and at least the stated size
+    need = lib.lp_sample_workspace_bytes(0, 2, 10)
+    assert need > 0
+    assert call(FAKE, 0, 2, 10, 10, ctypes.byref(p), out, None, WSN) == \
+        _lib.LP_ERR_INVALID_ARGUMENT
+    assert call(FAKE, 0, 2, 10, 10, ctypes.byref(p), out, WS, need - 1) == \
+        _lib.LP_ERR_INVALID_ARGUMENT
+    assert call(FAKE, 0, 2, 10, 10, ctypes.byref(p), out, ctypes.c_void_p(0x100010), WSN) == \
+        _lib.LP_ERR_INVALID_ARGUMENT
+
+
+def test_workspace_bytes(lib):
+    f = lib.lp_sample_workspace_bytes
+    assert f(0, 0, 1000) == 0
+    assert f(7, 4, 1000) == -1 and f(0, -1, 10) == -1 and f(0, 1, -1) == -1
+    for dt in (0, 1, 2):
+        sizes = [f(dt, B, V) for B, V in ((1, 1003), (64, 128256), (256, 131072), (1024, 202048))]
+        assert all(n > 0 and n % 256 == 0 for n in sizes)
+        assert sizes == sorted(sizes)  # more rows or tokens never need less
+    # bounded: tile summaries and slots are a few percent of the logits, the pool
+    # at most 128 MB
+    for dt, eb in ((0, 4), (2, 2)):
+        for B, V in ((1 << 20, 131072), (4096, 32000), (64, 1 << 24)):
+            assert f(dt, B, V) < B * V * eb * 7 // 100 + (130 << 20)
 
 
 def test_mask_and_sample_validation(lib):
@@ -135,13 +159,16 @@ def test_mask_and_sample_validation(lib):
     call = lambda **kw: lib.lp_mask_and_sample(  # noqa: E731
         kw.get("logits", FAKE), 2, kw.get("B", 4), kw.get("cols", 64), kw.get("stride", 64),
         kw.get("bm", FAKE), kw.get("bm_rows", 4), kw.get("words", 2), kw.get("bm_stride", 2),
-        kw.get("vocab", -1), kw.get("idx", None), kw.get("n", 0), ctypes.byref(p), out, None)
+        kw.get("vocab", -1), kw.get("idx", None), kw.get("n", 0), ctypes.byref(p), out,
+        kw.get("ws", WS), kw.get("wsn", WSN), None)
     assert call(vocab=65) == _lib.LP_ERR_INVALID_ARGUMENT
     assert call(bm_rows=3) == _lib.LP_ERR_INVALID_ARGUMENT
     assert call(n=2) == _lib.LP_ERR_INVALID_ARGUMENT
     assert call(bm_stride=1) == _lib.LP_ERR_INVALID_ARGUMENT
     assert call(stride=10) == _lib.LP_ERR_INVALID_ARGUMENT
     assert call(B=0) == _lib.LP_OK
+    assert call(ws=None) == _lib.LP_ERR_INVALID_ARGUMENT
+    assert call(wsn=16) == _lib.LP_ERR_INVALID_ARGUMENT
 
 
 def test_philox_validation(lib):

@@ -204,6 +204,28 @@ def test_small_workloads_parity():
     assert agree / total >= 0.999, agree / total
 
 
+def test_workspace_reuse_across_shapes():
+    """One workspace serves calls of any shape in any order: every call leaves
+    the state the next one needs (the counters at its front zero)."""
+    rng = np.random.default_rng(8)
+    ws = torch.zeros(ops.sample_workspace_bytes(torch.float32, 300, 70000), dtype=torch.uint8,
+                     device="cuda")
+    shapes = [(300, 1000), (2, 70000), (300, 70000), (17, 5000), (1, 64), (300, 33),
+              (150, 40000), (3, 1003)]
+    for rnd in range(2):
+        for i, (B, V) in enumerate(shapes):
+            x = (rng.standard_normal((B, V)) * 2).astype(np.float32)
+            args = dict(temperature=0.8, top_k=30, top_p=0.9, min_p=0.02)
+            own = (i + rnd) % 2 == 0
+            g = ops.sample(torch.from_numpy(x).cuda(), seed=rnd, offset=B, **args,
+                           workspace=ws if own else None).cpu().numpy()
+            w = syn.Workload("ws", "f32", x, V, V, seed=rnd)
+            w.temperature, w.top_k, w.top_p, w.min_p = 0.8, 30, 0.9, 0.02
+            check_rows(w, B, g, min_agree=0.98)
+    torch.cuda.synchronize()
+    assert int(ws[:256 + 4 * 16384].count_nonzero()) == 0
+
+
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
 def test_filter_grid_parity(dtype):
     """Every combination of filters, on rows narrow and flat, masked and not,
