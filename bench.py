@@ -193,6 +193,12 @@ def reduce_max(value: float, device=None) -> float:
     return float(t.item())
 
 
+def whole_job_rate(units_per_rank: float, world: int, seconds: float) -> float:
+    """Units processed by all ranks per second of the slowest rank (each rank runs
+    the same per-rank workload: weak scaling)."""
+    return units_per_rank * world / seconds
+
+
 def barrier():
     import torch.distributed as dist
 
@@ -466,10 +472,12 @@ def run_gpu(args) -> dict | None:
         kname = "apply_kernel" if op.kind == "apply" else "sample_kernel"
         rf = roofline(op.bytes, sec, peak, ncu_traffic(kname, wl))
         if op.kind == "apply":
-            lines["apply"] = {"value": round(op.bytes * ws / sec / 1e9, 2), "unit": "GB/s",
+            lines["apply"] = {"value": round(whole_job_rate(op.bytes, ws, sec) / 1e9, 2),
+                              "unit": "GB/s",
                               "workload": describe(op.w), "roofline": rf}
         else:
-            lines["sample"] = {"value": round(op.units * ws / sec, 1), "unit": "rows/s",
+            lines["sample"] = {"value": round(whole_job_rate(op.units, ws, sec), 1),
+                               "unit": "rows/s",
                                "workload": describe(op.w), "roofline": rf,
                                "GBps_algorithmic": rf["achieved"]}
     if "apply" in lines:
