@@ -67,7 +67,8 @@ static_assert(kPerPiece * 16 * kConsumers == kPieceBytes, "a piece is whole vect
 constexpr int kTileBytesMax = 32768;     // longest tile
 constexpr int kTileBytesMin = 8192;      // shortest tile (small batches)
 constexpr int64_t kTileTarget = 1024;    // tiles per launch that shorter tiles aim for
-constexpr int kCap = 3072;               // compaction entries per tile (shared memory)
+constexpr int kCap = 4352;               // compaction entries in shared memory
+constexpr int kCapT = kCap / 2;          // per tile: the buffer is double-buffered by tile parity
 constexpr int kSlotCap = 256;            // entries a tile keeps in its own workspace slot
 constexpr int kStage = 4096;             // buffered entries a finishing CTA stages
 constexpr int kMetaCap = 1024;           // tiles per row whose buffer starts it stages
@@ -396,20 +397,6 @@ __device__ __forceinline__ bool row_masked(const SampleArgs& a, int row) {
 
 // ================================================================ stream kernel
 
-// Consumer-only barriers (named barrier 1; the producer warp never joins).
-__device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;\n" ::"n"(kConsumers) : "memory");
-}
-__device__ __forceinline__ int consumer_sync_or(int pred) {
-  int r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.s32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n"
-      " selp.s32 %0, 1, 0, q;\n}\n"
-      : "=r"(r)
-      : "r"(pred), "n"(kConsumers)
-      : "memory");
-  return r;
-}
 __device__ __forceinline__ void mbar_arrive(uint64_t* m) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(m)) : "memory");
 }
@@ -425,14 +412,17 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
   extern __shared__ __align__(16) unsigned char smem[];
   unsigned char* const ring = smem;
   unsigned char* const mring = smem + kRing * kPieceBytes;
-  float* const bval = reinterpret_cast<float*>(mring + kRing * kMaskSlot);
-  int* const bidx = reinterpret_cast<int*>(bval + kCap);
+  // compaction buffers, one per tile parity
+  float* const bval0 = reinterpret_cast<float*>(mring + kRing * kMaskSlot);
+  int* const bidx0 = reinterpret_cast<int*>(bval0 + 2 * kCapT);
 
-  __shared__ float red_f[kConsumerWarps], red_s[kConsumerWarps], red_b[kConsumerWarps];
-  __shared__ int red_i[kConsumerWarps], red_n[kConsumerWarps], red_bv[kConsumerWarps];
-  __shared__ int s_count, s_err;
-  __shared__ unsigned s_off, s_nf;
-  __shared__ unsigned s_runkey;
+  // Per-tile state, double-buffered by tile parity: the warps of a CTA finish a
+  // tile independently; the last one to finish it merges the warps' partial
+  // summaries, writes the tile out and readies the parity for tile it + 2.
+  __shared__ float red_f[2][kConsumerWarps], red_s[2][kConsumerWarps], red_b[2][kConsumerWarps];
+  __shared__ int red_i[2][kConsumerWarps], red_n[2][kConsumerWarps], red_bv[2][kConsumerWarps];
+  __shared__ int s_count[2], s_done[2], s_fresh[2], s_err;
+  __shared__ unsigned s_runkey[2];
   __shared__ __align__(8) uint64_t full[kRing];
   __shared__ __align__(8) uint64_t empty[kRing];
   __shared__ uint4 keep_tab[256];  // 16-bit types: per-word keep masks of 8 element bits
@@ -441,6 +431,12 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
 
   if (tid == 0) {
     s_err = 0;
+    for (int p = 0; p < 2; ++p) {
+      s_count[p] = 0;
+      s_done[p] = 0;
+      s_runkey[p] = 0u;
+      s_fresh[p] = p;  // parity p is ready for tile iteration p
+    }
     for (int r = 0; r < kRing; ++r) {
       mbar_init(&full[r], 1);
       mbar_init(&empty[r], kConsumerWarps);
@@ -456,10 +452,11 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
   grid_dependency_wait();
   __syncthreads();
 
-  const int64_t G = gridDim.x;
-  auto tile_of = [&](int it) { return int64_t(blockIdx.x) + it * G; };
-  auto row_of = [&](int64_t t) { return a.row0 + int(t / a.tpr); };
-  auto part_of = [&](int64_t t) { return int(t % a.tpr); };
+  // tiles per launch fit in 32 bits (at most kMaxTileSums)
+  const unsigned G = gridDim.x, ntiles = unsigned(a.ntiles), tpr = unsigned(a.tpr);
+  auto tile_of = [&](int it) { return blockIdx.x + unsigned(it) * G; };
+  auto row_of = [&](unsigned t) { return a.row0 + int(t / tpr); };
+  auto part_of = [&](unsigned t) { return int(t % tpr); };
 
   // ================================================================ producer
   // Warp kConsumerWarps copies the pieces of this CTA's tiles, in order, into
@@ -468,8 +465,8 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
   // copies on the slot's mbarrier.
   if (warp == kConsumerWarps) {
     uint32_t issued = 0;
-    for (int it = 0; tile_of(it) < a.ntiles; ++it) {
-      const int64_t tile = tile_of(it);
+    for (int it = 0; tile_of(it) < ntiles; ++it) {
+      const unsigned tile = tile_of(it);
       const int row = row_of(tile);
       bool masked = false;  // warp-uniform
       if (a.bitmask) {
@@ -488,20 +485,30 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
         if (issued >= uint32_t(kRing) &&
             !mbar_wait(&empty[slot], ((issued / kRing) - 1u) & 1u) && lane == 0)
           s_err = 1;  // the consumers are gone: copy nothing more
-        if (lane != 0) continue;
         int q0, q1;
         g.piece_vecs(j, q0, q1);
         const int v0 = max(q0, g.qf0), v1 = min(q1, g.qf1);
         const uint32_t vbytes = v1 > v0 ? uint32_t(16 * (v1 - v0)) : 0u;
         uint32_t mbytes = 0;
-        int m_lo = 0, m_hi = 0;
+        int base = 0, w1 = 0, m_lo = 0;
         if (g.masked) {
-          int w0, w1;
+          // The slot holds the piece's words [w0, w1) from the 16-byte aligned
+          // word base <= w0 on: the aligned interior by bulk copy, the (at most
+          // three) words at each edge by plain loads of lanes 1-6.
+          int w0, m_hi;
           g.piece_words(j, w0, w1);
           g.mask_interior(w0, w1, m_lo, m_hi);
+          base = w0 - int((reinterpret_cast<uintptr_t>(g.gmask + w0) & 15) >> 2);
           mbytes = uint32_t(4 * (m_hi - m_lo));
+          uint32_t* mslot = reinterpret_cast<uint32_t*>(mring + slot * kMaskSlot);
+          const int x = lane >= 1 && lane <= 3 ? w0 + lane - 1
+                        : lane >= 4 && lane <= 6 ? m_hi + lane - 4
+                                                 : -1;
+          if (x >= 0 && (lane <= 3 ? x < m_lo : x < w1)) mslot[x - base] = __ldg(g.gmask + x);
+          __syncwarp();  // the edge words are stored before lane 0's arrive publishes them
         }
-        pmeta[slot] = make_int4(q0, q1, m_lo, m_hi);  // published by the arrive below
+        if (lane != 0) continue;
+        pmeta[slot] = make_int4(q0, q1, base, w1);  // published by the arrive below
         pflag[slot] = (q0 >= g.qf0 && q1 <= g.qf1 ? 1 : 0) | (g.masked ? 2 : 0);
         if (*(volatile int*)&s_err) {  // a copy went missing: start no more (rows report -2)
           mbar_expect_tx(&full[slot], 0);
@@ -511,7 +518,9 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
         if (vbytes)
           bulk_load(ring + slot * kPieceBytes + 16 * (v0 - q0), g.g0 + 16 * v0, vbytes,
                     &full[slot]);
-        if (mbytes) bulk_load(mring + slot * kMaskSlot, g.gmask + m_lo, mbytes, &full[slot]);
+        if (mbytes)
+          bulk_load(mring + slot * kMaskSlot + 4 * (m_lo - base), g.gmask + m_lo, mbytes,
+                    &full[slot]);
       }
     }
     return;
@@ -521,27 +530,39 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
   const uint2 key = make_uint2(uint32_t(a.seed), uint32_t(a.seed >> 32));
   uint32_t consumed = 0, lost = 0;
   RawParams nxt{};  // the next tile's row parameters, loaded a tile ahead
-  if (tile_of(0) < a.ntiles) nxt = raw_params(a, row_of(tile_of(0)));
+  if (tile_of(0) < ntiles) nxt = raw_params(a, row_of(tile_of(0)));
 
-  for (int it = 0; tile_of(it) < a.ntiles; ++it) {
-    const int64_t tile = tile_of(it);
+  for (int it = 0; tile_of(it) < ntiles; ++it) {
+    const unsigned tile = tile_of(it);
     const int row = row_of(tile);
     const int lrow = row - a.row0;
-    consumer_sync();  // the previous tile's buffer is written out
-    if (tid == 0) {
-      s_count = 0;
-      s_runkey = 0u;
-    }
-    consumer_sync();
+    const int par = it & 1;
+    float* const bval = bval0 + par * kCapT;
+    int* const bidx = bidx0 + par * kCapT;
 
     Sp pt;
     pt.init_tile(a, row, part_of(tile), false);  // masked: from the first piece
     const RowParams rp = row_params(nxt);
-    if (tile_of(it + 1) < a.ntiles) nxt = raw_params(a, row_of(tile_of(it + 1)));
+    if (tile_of(it + 1) < ntiles) nxt = raw_params(a, row_of(tile_of(it + 1)));
     const float T = rp.T, c2 = rp.c2, delta = rp.delta;
+
+    // this parity's state is ready once the last warp of tile it - 2 has reset
+    // it (bounded wait; the warps of a CTA are at most a few pieces apart)
+    if (lane == 0) {
+      for (uint32_t t = 0; *(volatile int*)&s_fresh[par] != it; ++t) {
+        if (t > kMaxWaitTries * 64u) {
+          s_err = 1;
+          break;
+        }
+        __nanosleep(64);
+      }
+      __threadfence_block();
+    }
+    __syncwarp();
+
     // the largest running maximum the row's other tiles have published, read one
-    // piece ahead of its use (thread 0)
-    unsigned hint = 0u;
+    // piece ahead of its use (thread 0); the largest key this warp has published
+    unsigned hint = 0u, wpub = 0u;
 
     // ------------------------------------------------------ stream the tile
     float m = -INFINITY, sm = 0.f;  // running max and softmax sum relative to it
@@ -578,10 +599,18 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
         const uint32_t* mw = reinterpret_cast<const uint32_t*>(mring + slot * kMaskSlot);
         // vector q of this piece and its candidate bits
         const bool plain = whole && !pt.masked;  // every vector staged, every token a candidate
+        // whole vectors of an aligned span: a vector's bits sit in one staged word
+        const bool aligned = whole && pt.masked && pt.mis == 0;
         auto load = [&](int q, uint4& raw, uint32_t& cb) {
           if (plain) {
             raw = *reinterpret_cast<const uint4*>(data + 16 * (q - pm.x));
             cb = Sp::ALL;
+            return;
+          }
+          if (aligned) {
+            raw = *reinterpret_cast<const uint4*>(data + 16 * (q - pm.x));
+            const int i0 = q * EPV;
+            cb = (mw[(i0 >> 5) - pm.z] >> (i0 & 31)) & Sp::ALL;
             return;
           }
           const bool staged = whole || (q >= pt.qf0 && q < pt.qf1);
@@ -662,19 +691,21 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
           }
         }
         if constexpr (compact) {  // warp-uniform: append the piece's candidates within the window
-          float wm = m;
-#pragma unroll
-          for (int o = 16; o; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(kFullWarp, wm, o));
-          if (lane == 0 && wm > -INFINITY) atomicMax(&s_runkey, fkey(wm));
+          // the warp's running maximum as an order key (0: none yet), published to
+          // the CTA when it rises
+          const unsigned wk = __reduce_max_sync(kFullWarp, m > -INFINITY ? fkey(m) : 0u);
+          if (lane == 0 && wk > wpub) {
+            atomicMax(&s_runkey[par], wk);
+            wpub = wk;
+          }
           if (tid == 0) {  // exchange with the row's other tiles
-            if (j > 0 && hint) atomicMax(&s_runkey, hint);
-            const unsigned mine = *(volatile unsigned*)&s_runkey;
+            if (j > 0 && hint) atomicMax(&s_runkey[par], hint);
+            const unsigned mine = *(volatile unsigned*)&s_runkey[par];
             if (mine) atomicMax(&a.rowkey[lrow], mine);
             hint = *(volatile unsigned*)&a.rowkey[lrow];
           }
-          const unsigned rk = *(volatile unsigned*)&s_runkey;
-          const float rm = rk ? fmaxf(wm, key_float(rk)) : wm;
-          const float cut = __fsub_rd(rm, delta);
+          const unsigned rk = max(wk, *(volatile unsigned*)&s_runkey[par]);
+          const float cut = rk ? __fsub_rd(key_float(rk), delta) : -INFINITY;
 #pragma unroll
           for (int r = 0; r < kPerPiece; ++r) {
             // a lane without a vector has vms = -inf, which must not pass a cut of -inf
@@ -697,13 +728,13 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
               if (lane >= o) incl += y;
             }
             int pos = 0;
-            if (lane == 31) pos = atomicAdd(&s_count, incl);
+            if (lane == 31) pos = atomicAdd(&s_count[par], incl);
             pos = __shfl_sync(kFullWarp, pos, 31) + incl - n;
             const int i0 = (16 * q - pt.mis) / Sp::EB;
             while (pass) {
               const int e = __ffs(pass) - 1;
               pass &= pass - 1;
-              if (pos < kCap) {
+              if (pos < kCapT) {
                 bval[pos] = E::get(mv[r], e);
                 bidx[pos] = pt.start + i0 + e;
               }
@@ -714,55 +745,50 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);  // this warp is done with the slot
       }
-    };
-    switch (rp.greedy ? kModeGreedy
-            : rp.has_p ? kModeTopP
-            : rp.compact ? kModeFilter
-                         : kModeUnfiltered) {
-      case kModeGreedy: stream(std::integral_constant<int, kModeGreedy>{}); break;
-      case kModeTopP: stream(std::integral_constant<int, kModeTopP>{}); break;
-      case kModeFilter: stream(std::integral_constant<int, kModeFilter>{}); break;
-      default: stream(std::integral_constant<int, kModeUnfiltered>{}); break;
-    }
-    const bool has_p = rp.has_p, unfiltered = rp.unfiltered, compact = rp.compact;
 
-    // ------------------------------------------------------- tile summary
-    {
+      // ---------------------------------------------------- warp epilogue
       float wm = m, ws = sm, wb = best;
       int wv = targ, wn = cnt, wbv = bestv;
 #pragma unroll
       for (int o = 16; o; o >>= 1) {
         const float m2 = __shfl_xor_sync(kFullWarp, wm, o);
-        const float s2 = __shfl_xor_sync(kFullWarp, ws, o);
         const int v2 = __shfl_xor_sync(kFullWarp, wv, o);
         wn += __shfl_xor_sync(kFullWarp, wn, o);
-        row_combine(wm, wv, ws, m2, v2, s2, c2, has_p);
-        if (unfiltered) {
+        if constexpr (has_p) {
+          const float s2 = __shfl_xor_sync(kFullWarp, ws, o);
+          row_combine(wm, wv, ws, m2, v2, s2, c2, true);
+        } else {
+          arg_combine(wm, wv, m2, v2);
+        }
+        if constexpr (unfiltered) {
           const float b2 = __shfl_xor_sync(kFullWarp, wb, o);
           const int bv2 = __shfl_xor_sync(kFullWarp, wbv, o);
           arg_combine(wb, wbv, b2, bv2);
         }
       }
+      int last = 0;
       if (lane == 0) {
-        red_f[warp] = wm;
-        red_s[warp] = ws;
-        red_i[warp] = wv;
-        red_n[warp] = wn;
-        red_b[warp] = wb;
-        red_bv[warp] = wbv;
+        red_f[par][warp] = wm;
+        red_s[par][warp] = ws;
+        red_i[par][warp] = wv;
+        red_n[par][warp] = wn;
+        red_b[par][warp] = wb;
+        red_bv[par][warp] = wbv;
+        __threadfence_block();
+        last = atomicAdd(&s_done[par], 1) == kConsumerWarps - 1;
       }
-    }
-    const int cta_err = consumer_sync_or(!stream_ok || s_err != 0);
-    if (warp == 0) {
-      float wm = -INFINITY, ws = 0.f, wb = -INFINITY;
-      int wv = INT_MAX, wn = 0, wbv = INT_MAX;
+      if (!__shfl_sync(kFullWarp, last, 0)) return;
+      // ------------------------------- the last warp writes the tile out
+      __threadfence_block();  // the other warps' summaries and buffer entries
+      wm = -INFINITY, ws = 0.f, wb = -INFINITY;
+      wv = INT_MAX, wn = 0, wbv = INT_MAX;
       if (lane < kConsumerWarps) {
-        wm = red_f[lane];
-        ws = red_s[lane];
-        wv = red_i[lane];
-        wn = red_n[lane];
-        wb = red_b[lane];
-        wbv = red_bv[lane];
+        wm = red_f[par][lane];
+        ws = red_s[par][lane];
+        wv = red_i[par][lane];
+        wn = red_n[par][lane];
+        wb = red_b[par][lane];
+        wbv = red_bv[par][lane];
       }
 #pragma unroll
       for (int o = 4; o; o >>= 1) {
@@ -775,19 +801,61 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
         const int bv2 = __shfl_xor_sync(kFullWarp, wbv, o);
         arg_combine(wb, wbv, b2, bv2);
       }
-      if (lane == 0) {
-        // the buffer goes to the tile's slot, or to the pool when longer
-        const unsigned n = compact ? unsigned(s_count) : 0u;
-        unsigned nf = n, off = 0u;
-        if (n > unsigned(kCap)) {
-          nf = kTileOverflow;
-        } else if (n > unsigned(kSlotCap)) {
-          off = atomicAdd(&a.hdr->pool_used, n);
-          if (off > a.pool_cap || n > a.pool_cap - off) nf = kTileOverflow;
+      // Drop the entries below the final cut (the tile's maximum, or a larger one
+      // of the row, less the window): they were appended under a lower running
+      // maximum.  The survivors keep their order in the buffer.
+      unsigned n = 0u;
+      if constexpr (compact) {
+        const unsigned cnt_all = unsigned(*(volatile int*)&s_count[par]);
+        if (cnt_all <= unsigned(kCapT)) {
+          unsigned fk = wm > -INFINITY ? fkey(wm) : 0u;
+          fk = max(fk, *(volatile unsigned*)&s_runkey[par]);
+          const float fcut_t = fk ? __fsub_rd(key_float(fk), delta) : -INFINITY;
+          for (unsigned b0 = 0; b0 < cnt_all; b0 += 32) {
+            const unsigned i = b0 + lane;
+            float x = 0.f;
+            int v = 0;
+            const bool keep = i < cnt_all && (x = bval[i], v = bidx[i], x >= fcut_t);
+            const unsigned bal = __ballot_sync(kFullWarp, keep);
+            __syncwarp();  // every lane has read its entry before any is overwritten
+            if (keep) {
+              const unsigned pos = n + unsigned(__popc(bal & ((1u << lane) - 1u)));
+              bval[pos] = x;
+              bidx[pos] = v;
+            }
+            n += unsigned(__popc(bal));
+          }
+          __syncwarp();
+        } else {
+          n = cnt_all;  // overflowed: flagged below
         }
-        if (cta_err) nf |= kTileError;
-        s_off = off;
-        s_nf = nf;
+      }
+      // the buffer goes to the tile's slot, or to the pool when longer
+      unsigned nf = n, off = 0u;
+      if (lane == 0) {
+        if constexpr (compact) {
+          if (n > unsigned(kCapT)) {
+            nf = kTileOverflow;
+          } else if (n > unsigned(kSlotCap)) {
+            off = atomicAdd(&a.hdr->pool_used, n);
+            if (off > a.pool_cap || n > a.pool_cap - off) nf = kTileOverflow;
+          }
+        }
+        if (!stream_ok || *(volatile int*)&s_err) nf |= kTileError;
+      }
+      nf = __shfl_sync(kFullWarp, nf, 0);
+      off = __shfl_sync(kFullWarp, off, 0);
+      if (!(nf & (kTileOverflow | kTileError))) {
+        const bool in_slot = nf <= unsigned(kSlotCap);
+        float* dv = in_slot ? a.slot_val + size_t(tile) * kSlotCap : a.pool_val + off;
+        int* di = in_slot ? a.slot_idx + size_t(tile) * kSlotCap : a.pool_idx + off;
+        for (unsigned i = lane; i < nf; i += 32) {
+          dv[i] = bval[i];
+          di[i] = bidx[i];
+        }
+      }
+      __syncwarp();  // every lane is done with the buffer before it is handed on
+      if (lane == 0) {
         TileSum& t = a.ts[tile];
         t.max = wm;
         t.arg = wv;
@@ -798,18 +866,23 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
         t.off = off;
         t.nf = nf;
         if (compact && wm > -INFINITY) atomicMax(&a.rowkey[lrow], fkey(wm));
+        // ready this parity for tile it + 2
+        s_count[par] = 0;
+        s_runkey[par] = 0u;
+        s_done[par] = 0;
+        __threadfence_block();
+        *(volatile int*)&s_fresh[par] = it + 2;
       }
-    }
-    consumer_sync();
-    const unsigned nf = s_nf;
-    if (!(nf & (kTileOverflow | kTileError))) {
-      const bool in_slot = nf <= unsigned(kSlotCap);
-      float* dv = in_slot ? a.slot_val + tile * kSlotCap : a.pool_val + s_off;
-      int* di = in_slot ? a.slot_idx + tile * kSlotCap : a.pool_idx + s_off;
-      for (unsigned i = tid; i < nf; i += kConsumers) {
-        dv[i] = bval[i];
-        di[i] = bidx[i];
-      }
+      __syncwarp();
+    };
+    switch (rp.greedy ? kModeGreedy
+            : rp.has_p ? kModeTopP
+            : rp.compact ? kModeFilter
+                         : kModeUnfiltered) {
+      case kModeGreedy: stream(std::integral_constant<int, kModeGreedy>{}); break;
+      case kModeTopP: stream(std::integral_constant<int, kModeTopP>{}); break;
+      case kModeFilter: stream(std::integral_constant<int, kModeFilter>{}); break;
+      default: stream(std::integral_constant<int, kModeUnfiltered>{}); break;
     }
   }
 
@@ -987,8 +1060,10 @@ __global__ void __launch_bounds__(kThreads) sample_finish_kernel(const SampleArg
     D = fmaxf(D, 0.f) * 1.001f + 1e-3f;
     fcut = fmaxf(fcut, __fsub_rd(lmax, T * D));
   }
-  // the tiles' buffers hold every candidate in [lo_w, lmax]
-  const float lo_w = has_m ? fm : __fsub_ru(lmax, rp.delta);
+  // the tiles' buffers hold every candidate in [lo_w, lmax]: the compaction
+  // window is the narrowest of the filters' windows (with min-p alone it ends
+  // exactly at fm)
+  const float lo_w = __fsub_ru(lmax, rp.delta);
 
   // ------------------------------- stage the tiles' buffers in shared memory
   // Entry i of the row (tile order) sits in tile t with tstart[t] <= i <

@@ -204,6 +204,24 @@ def test_small_workloads_parity():
     assert agree / total >= 0.999, agree / total
 
 
+def test_min_p_below_a_narrower_window():
+    """min-p admits tokens below the narrower top-k window that the tiles
+    compact: the keep-set must still include them (here 2000 tied tokens just
+    below the window carry ~38% of the kept mass)."""
+    V, B = 12000, 64
+    row = np.full(V, -5.0, np.float32)
+    row[0] = 10.0                 # the maximum
+    row[1:1000] = 5.0             # inside the 6-logit top-k window
+    row[1000:3000] = 3.95         # below the window, above the min-p bound 3.8
+    x = np.tile(row, (B, 1))
+    args = dict(temperature=1.0, top_k=2500, min_p=float(np.exp(-6.2)))
+    w = syn.Workload("minp_gap", "f32", x, V, V, seed=4)
+    w.temperature, w.top_k, w.min_p = 1.0, 2500, args["min_p"]
+    for off in range(3):
+        g = ops.sample(torch.from_numpy(x).cuda(), seed=4, offset=off, **args).cpu().numpy()
+        check_rows(w, off, g, min_agree=0.999)
+
+
 def test_workspace_reuse_across_shapes():
     """One workspace serves calls of any shape in any order: every call leaves
     the state the next one needs (the counters at its front zero)."""
