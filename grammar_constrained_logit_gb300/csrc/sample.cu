@@ -601,22 +601,20 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
         const bool plain = whole && !pt.masked;  // every vector staged, every token a candidate
         // whole vectors of an aligned span: a vector's bits sit in one staged word
         const bool aligned = whole && pt.masked && pt.mis == 0;
+        // vector q of this piece (its staged copy already in raw) and its candidate bits
         auto load = [&](int q, uint4& raw, uint32_t& cb) {
           if (plain) {
-            raw = *reinterpret_cast<const uint4*>(data + 16 * (q - pm.x));
             cb = Sp::ALL;
             return;
           }
           if (aligned) {
-            raw = *reinterpret_cast<const uint4*>(data + 16 * (q - pm.x));
             const int i0 = q * EPV;
             cb = (mw[(i0 >> 5) - pm.z] >> (i0 & 31)) & Sp::ALL;
             return;
           }
-          const bool staged = whole || (q >= pt.qf0 && q < pt.qf1);
-          raw = staged ? *reinterpret_cast<const uint4*>(data + 16 * (q - pm.x)) : pt.gvec(q);
+          if (!whole && !(q >= pt.qf0 && q < pt.qf1)) raw = pt.gvec(q);  // a ragged edge
           int i0;
-          cb = (whole && !pt.masked) ? Sp::ALL : pt.bits(q, i0, mw, pm.z, pm.w);
+          cb = pt.bits(q, i0, mw, pm.z, pm.w);
         };
         // the vector with every non-candidate element replaced by -inf
         auto masked_vec = [&](const uint4& raw, uint32_t cb) -> uint4 {
@@ -636,10 +634,16 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
         uint4 mv[kPerPiece];
         uint32_t cbs[kPerPiece];
         float vms[kPerPiece];
+        // the staged vectors sit at fixed offsets of the slot: load them before the
+        // piece's geometry is known
+        uint4 stg[kPerPiece];
+#pragma unroll
+        for (int r = 0; r < kPerPiece; ++r)
+          stg[r] = *reinterpret_cast<const uint4*>(data + 16 * (r * kConsumers + tid));
 #pragma unroll
         for (int r = 0; r < kPerPiece; ++r) {
           const int q = pm.x + r * kConsumers + tid;
-          uint4 raw = make_uint4(0, 0, 0, 0);
+          uint4 raw = stg[r];
           uint32_t cb = 0;
           if (q < pm.y) load(q, raw, cb);
           cbs[r] = cb;
@@ -747,20 +751,24 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
       }
 
       // ---------------------------------------------------- warp epilogue
-      float wm = m, ws = sm, wb = best;
-      int wv = targ, wn = cnt, wbv = bestv;
+      // the warp's maximum, its lowest index and the count by redux; the softmax
+      // sum rescaled to the warp maximum and summed in a fixed tree
+      float wm, ws = sm, wb = best;
+      int wv, wbv = bestv;
+      int wn = int(__reduce_add_sync(kFullWarp, unsigned(cnt)));
+      {
+        const unsigned mk = __reduce_max_sync(kFullWarp, m > -INFINITY ? fkey(m) : 0u);
+        wm = mk ? key_float(mk) : -INFINITY;
+        wv = int(__reduce_min_sync(kFullWarp, unsigned(mk && m == wm ? targ : INT_MAX)));
+      }
+      if constexpr (has_p) {
+        ws = m > -INFINITY ? sm * ex2((m - wm) * c2) : 0.f;
 #pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        const float m2 = __shfl_xor_sync(kFullWarp, wm, o);
-        const int v2 = __shfl_xor_sync(kFullWarp, wv, o);
-        wn += __shfl_xor_sync(kFullWarp, wn, o);
-        if constexpr (has_p) {
-          const float s2 = __shfl_xor_sync(kFullWarp, ws, o);
-          row_combine(wm, wv, ws, m2, v2, s2, c2, true);
-        } else {
-          arg_combine(wm, wv, m2, v2);
-        }
-        if constexpr (unfiltered) {
+        for (int o = 16; o; o >>= 1) ws += __shfl_xor_sync(kFullWarp, ws, o);
+      }
+      if constexpr (unfiltered) {
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
           const float b2 = __shfl_xor_sync(kFullWarp, wb, o);
           const int bv2 = __shfl_xor_sync(kFullWarp, wbv, o);
           arg_combine(wb, wbv, b2, bv2);
