@@ -157,17 +157,23 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from a committed ncu capture, if it was taken on the
-    current kernel sources; else None."""
+def ncu_traffic(kernels, workload: str):
+    """DRAM bytes per launch of the given kernels (summed: one hot-path call), from
+    the committed ncu captures, if they were taken on the current kernel sources;
+    else None."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
     if d.get("source_hash") != kernel_source_hash():
         return None
-    e = d.get("kernels", {}).get(f"{kernel}:{workload}")
-    return None if e is None else e.get("dram_bytes_per_launch")
+    total = 0
+    for k in ([kernels] if isinstance(kernels, str) else kernels):
+        e = d.get("kernels", {}).get(f"{k}:{workload}")
+        if e is None:
+            return None
+        total += int(e["dram_bytes_per_launch"])
+    return total
 
 
 def make_workload(name: str) -> syn.Workload:
@@ -469,8 +475,9 @@ def run_gpu(args) -> dict | None:
     for op, t in zip(plan, per_op):
         sec = t / K
         wl = op.w.name
-        kname = "apply_kernel" if op.kind == "apply" else "sample_kernel"
-        rf = roofline(op.bytes, sec, peak, ncu_traffic(kname, wl))
+        knames = (["apply_kernel"] if op.kind == "apply" else
+                  ["sample_stream_kernel", "sample_finish_kernel"])
+        rf = roofline(op.bytes, sec, peak, ncu_traffic(knames, wl))
         if op.kind == "apply":
             lines["apply"] = {"value": round(whole_job_rate(op.bytes, ws, sec) / 1e9, 2),
                               "unit": "GB/s",
@@ -488,7 +495,9 @@ def run_gpu(args) -> dict | None:
         res["unit"] = "rows/s"
     dominant = max(zip(plan, per_op), key=lambda x: x[1])[0]
     res["roofline"] = lines["apply" if dominant.kind == "apply" else "sample"]["roofline"]
-    res["roofline"]["kernel"] = "apply_kernel" if dominant.kind == "apply" else "sample_kernel"
+    res["roofline"]["kernel"] = (
+        "apply_kernel" if dominant.kind == "apply" else
+        "lp_mask_and_sample call: sample_stream_kernel + sample_finish_kernel, timed together")
     if "apply" in lines:
         res["apply"] = lines["apply"]
     if "sample" in lines:
