@@ -18,8 +18,8 @@ LP_F32, LP_F16, LP_BF16 = 0, 1, 2
 LP_OK, LP_ERR_INVALID_ARGUMENT, LP_ERR_UNSUPPORTED_DTYPE, LP_ERR_CUDA, LP_ERR_TOO_LARGE = range(5)
 
 EXPORTS = ("lp_apply_token_bitmask", "lp_apply_packed_bitmask", "lp_sample",
-           "lp_mask_and_sample", "lp_sample_workspace_bytes", "lp_philox4x32_10",
-           "lp_status_string")
+           "lp_mask_and_sample", "lp_sample_workspace_bytes", "lp_mask_and_sample_noalloc",
+           "lp_philox4x32_10", "lp_status_string")
 
 
 class SamplingParams(ctypes.Structure):
@@ -57,6 +57,10 @@ def declare(lib) -> None:
     lib.lp_mask_and_sample.argtypes = [c_vp, c_i32, c_i64, c_i64, c_i64, c_vp, c_i64, c_i64,
                                        c_i64, c_i64, c_vp, c_i64, ctypes.POINTER(SamplingParams),
                                        c_vp, c_vp, c_i64, c_vp]
+    lib.lp_mask_and_sample_noalloc.restype = c_i32
+    lib.lp_mask_and_sample_noalloc.argtypes = [c_vp, c_i32, c_i64, c_i64, c_i64, c_vp, c_i64,
+                                               c_i64, c_i64, c_i64, c_vp, c_i64,
+                                               ctypes.POINTER(SamplingParams), c_vp, c_vp]
     lib.lp_sample_workspace_bytes.restype = c_i64
     lib.lp_sample_workspace_bytes.argtypes = [c_i32, c_i64, c_i64]
     lib.lp_philox4x32_10.restype = c_i32

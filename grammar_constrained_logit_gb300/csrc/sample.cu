@@ -1596,6 +1596,35 @@ extern "C" lp_status lp_mask_and_sample(const void* logits, lp_dtype dt, int64_t
                     workspace, workspace_bytes, stream);
 }
 
+// Device scratch of the module itself, for callers that pass no workspace: zero
+// when the module loads (the state lp_sample needs), and kept so by every call.
+namespace lp {
+namespace {
+constexpr int64_t kNoAllocBytes = int64_t(128) << 20;
+__device__ __align__(256) unsigned char g_noalloc_ws[kNoAllocBytes];
+}  // namespace
+}  // namespace lp
+
+extern "C" lp_status lp_mask_and_sample_noalloc(const void* logits, lp_dtype dt, int64_t B,
+                                                int64_t cols, int64_t logits_stride,
+                                                const int32_t* bitmask, int64_t bitmask_rows,
+                                                int64_t bitmask_words, int64_t bitmask_stride,
+                                                int64_t vocab_size, const int32_t* indices,
+                                                int64_t num_indices,
+                                                const lp_sampling_params* params,
+                                                int64_t* out_ids, cudaStream_t stream) {
+  if (!(dt == LP_F32 || dt == LP_F16 || dt == LP_BF16)) return LP_ERR_UNSUPPORTED_DTYPE;
+  if (B < 0 || cols < 0) return LP_ERR_INVALID_ARGUMENT;
+  if (B == 0) return LP_OK;
+  // the widest vocabulary the call can use sizes the scratch it needs
+  if (lp_sample_workspace_bytes(dt, B, cols) > kNoAllocBytes) return LP_ERR_TOO_LARGE;
+  void* ws = nullptr;
+  if (cudaGetSymbolAddress(&ws, g_noalloc_ws) != cudaSuccess) return LP_ERR_CUDA;
+  return lp_mask_and_sample(logits, dt, B, cols, logits_stride, bitmask, bitmask_rows,
+                            bitmask_words, bitmask_stride, vocab_size, indices, num_indices,
+                            params, out_ids, ws, kNoAllocBytes, stream);
+}
+
 extern "C" lp_status lp_philox4x32_10(const uint32_t* counters, const uint32_t* keys,
                                       uint32_t* out, int64_t n, cudaStream_t stream) {
   if (n < 0) return LP_ERR_INVALID_ARGUMENT;

@@ -183,6 +183,25 @@ lp_status lp_mask_and_sample(const void* logits, lp_dtype dt, int64_t B, int64_t
                              void* workspace, int64_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * lp_mask_and_sample_noalloc -- lp_mask_and_sample with no caller workspace: the
+ * call uses a 128 MiB device array that the library itself holds (allocated and
+ * zero-filled when the library's module loads).  The pages have no counterpart;
+ * it exists for callers that cannot allocate scratch.  Arguments, results and
+ * errors as lp_mask_and_sample, plus LP_ERR_TOO_LARGE when
+ * lp_sample_workspace_bytes(dt, B, cols) exceeds 128 MiB.  All calls of a
+ * process share the one array, so they must be ordered (one stream, or
+ * events): two such calls in flight at once on different streams are invalid
+ * and not detected.
+ */
+lp_status lp_mask_and_sample_noalloc(const void* logits, lp_dtype dt, int64_t B, int64_t cols,
+                                     int64_t logits_stride, const int32_t* bitmask,
+                                     int64_t bitmask_rows, int64_t bitmask_words,
+                                     int64_t bitmask_stride, int64_t vocab_size,
+                                     const int32_t* indices, int64_t num_indices,
+                                     const lp_sampling_params* params, int64_t* out_ids,
+                                     cudaStream_t stream);
+
+/*
  * lp_philox4x32_10 -- diagnostic: the device's Philox4x32-10 (Salmon et al.,
  * SC'11, 10 rounds) evaluated on n caller-given blocks, so tests can compare the
  * noise stream of lp_sample word for word.
