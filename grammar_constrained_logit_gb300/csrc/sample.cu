@@ -71,6 +71,8 @@ constexpr int kCap = 4352;               // compaction entries in shared memory
 constexpr int kCapT = kCap / 2;          // per tile: the buffer is double-buffered by tile parity
 constexpr int kSlotCap = 256;            // entries a tile keeps in its own workspace slot
 constexpr int kStage = 4096;             // buffered entries a finishing CTA stages
+constexpr int kWinBins = 256;            // bins of the fallback's window search (one per thread)
+static_assert(kWinBins == kThreads, "one window bin per thread");
 constexpr int kMetaCap = 1024;           // tiles per row whose buffer starts it stages
 constexpr int kFinishSmem = kStage * 8 + (kMetaCap + 1) * 4;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -903,7 +905,7 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
 // ================================================================ finish kernel
 
 template <int DT>
-__global__ void __launch_bounds__(kThreads) sample_finish_kernel(const SampleArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const SampleArgs a) {
   using E = Elt<DT>;
   using Sp = Span<DT>;
   constexpr int EPV = E::kPerVec;
@@ -1197,15 +1199,17 @@ __global__ void __launch_bounds__(kThreads) sample_finish_kernel(const SampleArg
   // Largest key x >= key(lo) with count(>= x) >= k (top-k) or mass(>= x) >= P
   // (top-p), counting candidates of the tiles' buffers or of a re-read of the
   // row.  False when none exists.
-  auto descend = [&](bool from_buffers, float lo, uint32_t& out_key) -> bool {
-    const uint32_t klo = fkey(lo), khi = fkey(lmax);
+  // Over [lo, hi], with above_c0 / above_m0 already counted above hi.
+  auto descend = [&](bool from_buffers, float lo, uint32_t& out_key, float hi = INFINITY,
+                     unsigned above_c0 = 0u, unsigned long long above_m0 = 0ull) -> bool {
+    const uint32_t klo = fkey(lo), khi = fkey(fminf(hi, lmax));
     const uint32_t diff = klo ^ khi;
     int top = diff ? 32 - __clz(diff) : kLow + 1;  // one past the highest differing bit
     top = max(top, kLow + 1);
     int shift = max(top - 8, kLow);
     uint32_t prefix = top >= 32 ? 0u : khi & ~((1u << top) - 1u);
-    unsigned above_c = 0;
-    unsigned long long above_m = 0;
+    unsigned above_c = above_c0;
+    unsigned long long above_m = above_m0;
     for (;;) {
       const int hp = npass & 1;
       ++npass;
@@ -1296,6 +1300,131 @@ __global__ void __launch_bounds__(kThreads) sample_finish_kernel(const SampleArg
     }
   };
 
+
+  // ---------------------- a window around the threshold (top-p rows, re-read)
+  // For float32 logits (four radix passes over the row), two re-reads of the row
+  // stand in for a radix pass per key digit.  The first
+  // sums the candidates' softmax mass and count in kWinBins equal bins of
+  // (lmax - x) / T down to fcut (per-warp bins, fp32 sums); the bin where the
+  // cumulative mass (or count, for top-k) reaches its target bounds, with one bin
+  // of margin each side, a window [lo2, hi2).  The second sums the exact count
+  // and fixed-point mass above hi2 and stages the window's candidates; the exact
+  // descent over them, started from those sums, gives the threshold.  False when
+  // the window misses it or does not fit (the caller then descends the whole row).
+  auto window_select = [&](uint32_t& out_key) -> bool {
+    // 16-bit keys need at most two radix passes: the window saves nothing there
+    if (Sp::EB != 4) return false;
+    if (!has_p || !(fcut > -INFINITY) || !(lmax > fcut)) return false;
+    const float zspan = (lmax - fcut) / T;                 // scaled width of [fcut, lmax]
+    const float bpl = float(kWinBins) / (zspan * T);       // bins per logit
+    float* wmass = reinterpret_cast<float*>(fsmem);        // [kWarps][kWinBins]
+    unsigned* wcnt = reinterpret_cast<unsigned*>(wmass + kWarps * kWinBins);
+    for (int i = tid; i < kWarps * kWinBins; i += kThreads) {
+      wmass[i] = 0.f;
+      wcnt[i] = 0u;
+    }
+    __syncthreads();
+    reread([&](const uint4& raw, uint32_t cb, int) {
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        const float x = E::get(raw, e);
+        if (!((cb >> e) & 1u) || !(x >= fcut)) continue;
+        const int b = min(max(int((lmax - x) * bpl), 0), kWinBins - 1);
+        atomicAdd(&wmass[warp * kWinBins + b], ex2((x - lmax) * c2));
+        atomicAdd(&wcnt[warp * kWinBins + b], 1u);
+      }
+    });
+    __syncthreads();
+    // bin tid (0 = next to the maximum): totals, then an inclusive scan over bins
+    double cm = 0.0;  // the bins' sums carry fp32 rounding; the window's margin absorbs it
+    unsigned cc = 0u;
+    for (int w = 0; w < kWarps; ++w) {
+      cm += double(wmass[w * kWinBins + tid]);
+      cc += wcnt[w * kWinBins + tid];
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double ym = __shfl_up_sync(kFullWarp, cm, o);
+      const unsigned yc = __shfl_up_sync(kFullWarp, cc, o);
+      if (lane >= o) {
+        cm += ym;
+        cc += yc;
+      }
+    }
+    __shared__ double s_wm[kWarps];
+    __shared__ unsigned s_wc[kWarps];
+    if (lane == 31) {
+      s_wm[warp] = cm;
+      s_wc[warp] = cc;
+    }
+    if (tid == 0) s_sel = INT_MAX;
+    __syncthreads();
+    for (int w = 0; w < warp; ++w) {
+      cm += s_wm[w];
+      cc += s_wc[w];
+    }
+    const double target_m = double(fmaxf(rp.tp, 0.f)) * double(S);
+    if (cm >= target_m || (has_k && cc >= unsigned(k))) atomicMin(&s_sel, tid);
+    __syncthreads();
+    const int bt = s_sel;
+    if (bt == INT_MAX) return false;
+    // the window: bins [bt - 1, bt + 1], as logits
+    const float hi2 = bt >= 2 ? __fadd_ru(lmax, -float(bt - 1) / bpl) : INFINITY;
+    const float lo2 = fmaxf(__fadd_rd(lmax, -float(bt + 2) / bpl), fcut);
+    // exact count and mass above the window; the window's candidates staged
+    unsigned ca = 0u;
+    unsigned long long ma = 0ull;
+    if (tid == 0) s_nst = 0u;
+    __syncthreads();
+    reread([&](const uint4& raw, uint32_t cb, int i0) {
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        const float x = E::get(raw, e);
+        const bool cand = ((cb >> e) & 1u) && x > -INFINITY;
+        if (cand && x >= hi2) {
+          ++ca;
+          ma += __float2ull_rn(ex2((x - lmax) * c2) * 1099511627776.0f);
+        }
+        const bool in = cand && x >= lo2 && x < hi2;
+        const unsigned bal = __ballot_sync(kFullWarp, in);
+        unsigned base = 0u;
+        if (lane == 0 && bal) base = atomicAdd(&s_nst, unsigned(__popc(bal)));
+        base = __shfl_sync(kFullWarp, base, 0);
+        if (in) {
+          const unsigned pos = base + unsigned(__popc(bal & ((1u << lane) - 1u)));
+          if (pos < unsigned(kStage)) {
+            bval[pos] = x;
+            bidx[pos] = rw.start + i0 + e;
+          }
+        }
+      }
+    });
+    // block sums of the exact counts above the window
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      ca += __shfl_xor_sync(kFullWarp, ca, o);
+      ma += __shfl_xor_sync(kFullWarp, ma, o);
+    }
+    if (lane == 0) {
+      scan_c[warp] = ca;
+      scan_m[warp] = ma;
+    }
+    __syncthreads();
+    ca = 0u;
+    ma = 0ull;
+    for (int w = 0; w < kWarps; ++w) {
+      ca += scan_c[w];
+      ma += scan_m[w];
+    }
+    const unsigned nwin = s_nst;
+    __syncthreads();
+    if (nwin > unsigned(kStage)) return false;
+    if ((has_k && ca >= unsigned(k)) || ma >= P) return false;  // the threshold is above
+    staged = true;
+    nst = nwin;
+    return descend(true, lo2, out_key, hi2, ca, ma);
+  };
+
   float thr = fm;
   bool from_buffers = !any_overflow;
   if (has_k || has_p) {
@@ -1305,7 +1434,7 @@ __global__ void __launch_bounds__(kThreads) sample_finish_kernel(const SampleArg
       found = descend(true, lo_b, kx);
       if (!found && !(fm >= lo_b)) from_buffers = false;
     }
-    if (!from_buffers) found = descend(false, fcut, kx);
+    if (!from_buffers) found = window_select(kx) || descend(false, fcut, kx);
     if (found) thr = fmaxf(key_float(kx), fm);
   } else if (from_buffers && !(fm >= lo_w)) {
     from_buffers = false;
