@@ -664,11 +664,12 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
         if (pmx > m) {  // a new running maximum: its lowest index in this piece
           if constexpr (has_p) sm *= ex2((m - pmx) * c2);  // 0 while m is still -inf
           m = pmx;
+          const uint4 best_v = rmx == 0 ? mv[0] : mv[kPerPiece - 1];
           const int q = pm.x + rmx * kConsumers + tid;
           const int i0 = (16 * q - pt.mis) / Sp::EB;
 #pragma unroll
           for (int e = EPV - 1; e >= 0; --e)
-            if (E::get(mv[rmx], e) == pmx) targ = pt.start + i0 + e;
+            if (E::get(best_v, e) == pmx) targ = pt.start + i0 + e;
         }
         if constexpr (has_p) {  // -inf elements add 0 (m is finite once any candidate is seen)
           const float off = m * c2;

@@ -172,9 +172,12 @@ def sample_workspace_bytes(dtype: torch.dtype, batch_size: int, vocab_size: int)
 
 
 def _workspace(workspace, lg: torch.Tensor, B: int, vocab: int):
-    """The caller's workspace (a zero-filled uint8 CUDA tensor), or one kept per
-    (device, stream), grown on demand.  The library leaves it zero-filled after
-    every call.  Returns (pointer, bytes)."""
+    """The caller's workspace (a uint8 CUDA tensor, zero-filled before its first
+    use), or one kept per (device, stream), grown on demand; the library keeps its
+    counters valid across calls.  When capturing a CUDA graph, pass an explicit
+    workspace allocated before the capture: the capture stream would otherwise get
+    a workspace of its own allocated (and zero-filled) inside the graph.
+    Returns (pointer, bytes)."""
     need = sample_workspace_bytes(lg.dtype, B, max(vocab, 0))
     if workspace is not None:
         if workspace.dtype != torch.uint8 or not workspace.is_contiguous() or \
