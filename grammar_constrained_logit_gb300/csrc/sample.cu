@@ -79,6 +79,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kWindowK = 6.f;          // top-k window, in logits
 constexpr int kSmem = kRing * kPieceBytes + kRing * kMaskSlot + kCap * 8;
 constexpr uint32_t kMaxWaitTries = 1u << 22;
+constexpr int kTestWaits = 8;            // non-blocking tests before an mbarrier wait suspends
 constexpr int64_t kMaxTileSums = int64_t(1) << 20;  // tiles per launch
 constexpr int64_t kMaxRowsPerLaunch = 16384;
 constexpr int64_t kPoolPerRow = 8192;    // pooled compaction entries per row
@@ -265,10 +266,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* m, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait for the phase of the given parity to complete.  Each try_wait
-// suspends the thread for a hardware-chosen time slice; after kMaxWaitTries
-// failures (far beyond any copy's latency) it gives up and returns false.
+// Non-blocking test of the phase of the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* m, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(m)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase of the given parity to complete: a few
+// non-blocking tests first (a phase that completes soon is seen without a
+// suspend and wake-up), then try_wait, which suspends the thread for a
+// hardware-chosen time slice; after kMaxWaitTries failures (far beyond any
+// copy's latency) it gives up and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* m, uint32_t parity) {
+  for (int i = 0; i < kTestWaits; ++i)
+    if (mbar_test_wait(m, parity)) return true;
   for (uint32_t i = 0; i < kMaxWaitTries; ++i)
     if (mbar_try_wait(m, parity)) return true;
   return false;
