@@ -6,12 +6,12 @@
 //
 // The stream kernel makes the one pass over HBM, through the Tensor Memory
 // Accelerator, in a persistent grid of three CTAs per SM.  Every row is cut into
-// tiles of equal length (8-32 KB of logits) and the CTAs take the tiles of all
+// tiles of equal length (8-64 KB of logits) and the CTAs take the tiles of all
 // rows round-robin, so the work per SM is even whatever the batch size and
-// vocabulary.  A CTA streams its tiles through a ring of four 8 KB
-// shared-memory stages: one thread keeps bulk copies (cp.async.bulk, with the
-// stage's bitmask words) in flight on mbarriers, running up to one tile ahead,
-// and the 256 threads consume each landed stage from shared memory.  Per tile:
+// vocabulary.  A CTA streams its tiles through a ring of four 7 KB
+// shared-memory stages: a producer warp keeps bulk copies (cp.async.bulk, with
+// the stage's bitmask words) in flight on mbarriers, and seven consumer warps
+// take each landed stage from shared memory.  Per tile:
 //   * candidate max with its lowest index, the candidate count and, for top-p
 //     rows, an online softmax sum;
 //   * filtered rows: every candidate within a window below the tile's running
@@ -58,17 +58,16 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kConsumerWarps = kWarps - 1;  // stream kernel: the last warp is the producer
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kRing = 4;                 // stages in flight per CTA
-constexpr int kPieceBytes = 7168;        // bytes of logits per stage: two vectors per consumer
+constexpr int kRing = 3;                 // stages in flight per CTA
+constexpr int kPieceBytes = 14336;       // bytes of logits per stage: four vectors per consumer
 constexpr int kPieceWords = kPieceBytes / 2 / 32 + 2;  // bitmask words a stage can need
 constexpr int kMaskSlot = (16 + 4 * kPieceWords + 15) / 16 * 16;
 constexpr int kPerPiece = kPieceBytes / 16 / kConsumers;  // vectors of a piece per consumer
 static_assert(kPerPiece * 16 * kConsumers == kPieceBytes, "a piece is whole vectors per consumer");
-constexpr int kTileBytesMax = 32768;     // longest tile
+constexpr int kTileBytesMax = 65536;     // longest tile
 constexpr int kTileBytesMin = 8192;      // shortest tile (small batches)
 constexpr int64_t kTileTarget = 1024;    // tiles per launch that shorter tiles aim for
-constexpr int kCap = 4352;               // compaction entries in shared memory
-constexpr int kCapT = kCap / 2;          // per tile: the buffer is double-buffered by tile parity
+constexpr int kCompactBytes = 24576;     // shared memory of the compaction buffers
 constexpr int kSlotCap = 256;            // entries a tile keeps in its own workspace slot
 constexpr int kStage = 4096;             // buffered entries a finishing CTA stages
 constexpr int kWinBins = 256;            // bins of the fallback's window search (one per thread)
@@ -77,7 +76,31 @@ constexpr int kMetaCap = 1024;           // tiles per row whose buffer starts it
 constexpr int kFinishSmem = kStage * 8 + (kMetaCap + 1) * 4;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kWindowK = 6.f;          // top-k window, in logits
-constexpr int kSmem = kRing * kPieceBytes + kRing * kMaskSlot + kCap * 8;
+constexpr int kSmem = kRing * kPieceBytes + kRing * kMaskSlot + kCompactBytes;
+// A compaction entry is the logit's own bits (4 or 2 bytes) and the token's
+// offset into the tile (2 bytes); the buffer is double-buffered by tile parity.
+static_assert(kTileBytesMax / 2 <= 65536, "tile offsets fit in 16 bits");
+template <int DT>
+struct Compact {
+  using Val = std::conditional_t<DT == LP_F32, float, uint16_t>;
+  static constexpr int kCapT = kCompactBytes / 2 / int(sizeof(Val) + 2);  // entries per tile
+  __device__ static __forceinline__ Val pack(const uint4& v, int e) {
+    if constexpr (DT == LP_F32) {
+      return Elt<DT>::get(v, e);
+    } else {
+      return uint16_t(word_of(v, e >> 1) >> (16 * (e & 1)));
+    }
+  }
+  __device__ static __forceinline__ float unpack(Val x) {
+    if constexpr (DT == LP_F32) {
+      return x;
+    } else if constexpr (DT == LP_BF16) {
+      return __uint_as_float(uint32_t(x) << 16);
+    } else {
+      return Elt<LP_F16>::half_bits_to_float(x);
+    }
+  }
+};
 constexpr uint32_t kMaxWaitTries = 1u << 22;
 constexpr int kTestWaits = 8;            // non-blocking tests before an mbarrier wait suspends
 constexpr int64_t kMaxTileSums = int64_t(1) << 20;  // tiles per launch
@@ -430,9 +453,13 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
   extern __shared__ __align__(16) unsigned char smem[];
   unsigned char* const ring = smem;
   unsigned char* const mring = smem + kRing * kPieceBytes;
-  // compaction buffers, one per tile parity
-  float* const bval0 = reinterpret_cast<float*>(mring + kRing * kMaskSlot);
-  int* const bidx0 = reinterpret_cast<int*>(bval0 + 2 * kCapT);
+  // compaction buffers, one per tile parity: the value and the token's offset
+  // into the tile
+  using Cp = Compact<DT>;
+  using CVal = typename Cp::Val;
+  constexpr int kCapT = Cp::kCapT;
+  CVal* const bval0 = reinterpret_cast<CVal*>(mring + kRing * kMaskSlot);
+  uint16_t* const bidx0 = reinterpret_cast<uint16_t*>(bval0 + 2 * kCapT);
 
   // Per-tile state, double-buffered by tile parity: the warps of a CTA finish a
   // tile independently; the last one to finish it merges the warps' partial
@@ -555,8 +582,8 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
     const int row = row_of(tile);
     const int lrow = row - a.row0;
     const int par = it & 1;
-    float* const bval = bval0 + par * kCapT;
-    int* const bidx = bidx0 + par * kCapT;
+    CVal* const bval = bval0 + par * kCapT;
+    uint16_t* const bidx = bidx0 + par * kCapT;
 
     Sp pt;
     pt.init_tile(a, row, part_of(tile), false);  // masked: from the first piece
@@ -680,7 +707,10 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
         if (pmx > m) {  // a new running maximum: its lowest index in this piece
           if constexpr (has_p) sm *= ex2((m - pmx) * c2);  // 0 while m is still -inf
           m = pmx;
-          const uint4 best_v = rmx == 0 ? mv[0] : mv[kPerPiece - 1];
+          uint4 best_v = mv[0];  // mv[rmx], without a run-time index
+#pragma unroll
+          for (int r = 1; r < kPerPiece; ++r)
+            if (rmx == r) best_v = mv[r];
           const int q = pm.x + rmx * kConsumers + tid;
           const int i0 = (16 * q - pt.mis) / Sp::EB;
 #pragma unroll
@@ -697,12 +727,14 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
           }
         }
         if constexpr (unfiltered) {
+          // the element loop is not unrolled: each Gumbel score inlines a Philox
+          // block, and one copy per vector keeps the kernel's code small
 #pragma unroll
           for (int r = 0; r < kPerPiece; ++r) {
             if (!cbs[r]) continue;
             const int q = pm.x + r * kConsumers + tid;
             const int i0 = (16 * q - pt.mis) / Sp::EB;
-#pragma unroll
+#pragma unroll 1
             for (int e = 0; e < EPV; ++e) {
               const float x = E::get(mv[r], e);
               if (!(x > -INFINITY)) continue;
@@ -758,8 +790,8 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
               const int e = __ffs(pass) - 1;
               pass &= pass - 1;
               if (pos < kCapT) {
-                bval[pos] = E::get(mv[r], e);
-                bidx[pos] = pt.start + i0 + e;
+                bval[pos] = Cp::pack(mv[r], e);
+                bidx[pos] = uint16_t(i0 + e);
               }
               ++pos;
             }
@@ -840,9 +872,10 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
           const float fcut_t = fk ? __fsub_rd(key_float(fk), delta) : -INFINITY;
           for (unsigned b0 = 0; b0 < cnt_all; b0 += 32) {
             const unsigned i = b0 + lane;
-            float x = 0.f;
-            int v = 0;
-            const bool keep = i < cnt_all && (x = bval[i], v = bidx[i], x >= fcut_t);
+            CVal x{};
+            uint16_t v = 0;
+            const bool keep =
+                i < cnt_all && (x = bval[i], v = bidx[i], Cp::unpack(x) >= fcut_t);
             const unsigned bal = __ballot_sync(kFullWarp, keep);
             __syncwarp();  // every lane has read its entry before any is overwritten
             if (keep) {
@@ -877,8 +910,8 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
         float* dv = in_slot ? a.slot_val + size_t(tile) * kSlotCap : a.pool_val + off;
         int* di = in_slot ? a.slot_idx + size_t(tile) * kSlotCap : a.pool_idx + off;
         for (unsigned i = lane; i < nf; i += 32) {
-          dv[i] = bval[i];
-          di[i] = bidx[i];
+          dv[i] = Cp::unpack(bval[i]);
+          di[i] = pt.start + int(bidx[i]);
         }
       }
       __syncwarp();  // every lane is done with the buffer before it is handed on
