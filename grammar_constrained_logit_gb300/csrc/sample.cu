@@ -954,6 +954,45 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
 
 // ================================================================ finish kernel
 
+// What a filtered row's merged summary fixes before any selection: the top-k
+// that still filters, the min-p cut fm, a certified lower bound fcut of the
+// keep-threshold, the lowest logit lo_w down to which the tiles' buffers hold
+// every candidate, and the top-p mass target P in 2^-40 units.
+struct RowBounds {
+  int k;
+  bool has_k;
+  float fm, fcut, lo_w;
+  unsigned long long P;
+};
+__device__ __forceinline__ RowBounds row_bounds(const RowParams& rp, float lmax, float S,
+                                                int ncand_ub) {
+  RowBounds b;
+  b.k = rp.k;
+  if (b.k > 0 && b.k >= ncand_ub) b.k = 0;  // keeps every candidate
+  b.has_k = b.k > 0;
+  b.fm = rp.has_m ? fminf(__fadd_ru(lmax, rp.tl), lmax) : -INFINITY;
+  b.fcut = b.fm;
+  if (rp.has_p) {  // t_p >= (1 - top_p) / ncand, as a logit
+    float D = logf(float(ncand_ub) / (fmaxf(1.f - rp.tp, 1e-30f) * S));
+    D = fmaxf(D, 0.f) * 1.001f + 1e-3f;
+    b.fcut = fmaxf(b.fcut, __fsub_rd(lmax, rp.T * D));
+  }
+  // the compaction window is the narrowest of the filters' windows (with min-p
+  // alone it ends exactly at fm)
+  b.lo_w = __fsub_ru(lmax, rp.delta);
+  b.P = 0ull;
+  if (rp.has_p) {
+    const float t = fmaxf(rp.tp, 0.f) * S * 1099511627776.0f;
+    b.P = t >= 1.8e19f ? ~0ull : static_cast<unsigned long long>(t);
+  }
+  return b;
+}
+
+// Softmax mass of logit x in 2^-40 units (x <= lmax), as every selection counts it.
+__device__ __forceinline__ unsigned long long mass40(float x, float lmax, float c2) {
+  return __float2ull_rn(ex2((x - lmax) * c2) * 1099511627776.0f);
+}
+
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const SampleArgs a) {
   using E = Elt<DT>;
@@ -987,7 +1026,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
   const uint2 key = make_uint2(uint32_t(a.seed), uint32_t(a.seed >> 32));
   const RowParams rp = row_params(raw_params(a, row));
   const float T = rp.T, c2 = rp.c2;
-  const bool has_p = rp.has_p, has_m = rp.has_m;
+  const bool has_p = rp.has_p;
   const int64_t t0 = int64_t(lrow) * a.tpr;
   const TileSum* rts = a.ts + t0;
   const bool meta = a.tpr <= kMetaCap;  // tile starts of the staged buffer fit
@@ -1110,20 +1149,11 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
   }
 
   // ------------------------------------------------------- filter bounds
-  int k = rp.k;
-  if (k > 0 && k >= ncand_ub) k = 0;  // keeps every candidate
-  const bool has_k = k > 0;
-  const float fm = has_m ? fminf(__fadd_ru(lmax, rp.tl), lmax) : -INFINITY;
-  float fcut = fm;  // certified lower bound of the keep-threshold
-  if (has_p) {
-    float D = logf(float(ncand_ub) / (fmaxf(1.f - rp.tp, 1e-30f) * S));
-    D = fmaxf(D, 0.f) * 1.001f + 1e-3f;
-    fcut = fmaxf(fcut, __fsub_rd(lmax, T * D));
-  }
-  // the tiles' buffers hold every candidate in [lo_w, lmax]: the compaction
-  // window is the narrowest of the filters' windows (with min-p alone it ends
-  // exactly at fm)
-  const float lo_w = __fsub_ru(lmax, rp.delta);
+  const RowBounds bd = row_bounds(rp, lmax, S, ncand_ub);
+  const int k = bd.k;
+  const bool has_k = bd.has_k;
+  const float fm = bd.fm, fcut = bd.fcut;
+  const float lo_w = bd.lo_w;  // the tiles' buffers hold every candidate in [lo_w, lmax]
 
   // ------------------------------- stage the tiles' buffers in shared memory
   // Entry i of the row (tile order) sits in tile t with tstart[t] <= i <
@@ -1240,11 +1270,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
   };
 
   // ---------------------------------- radix select of the threshold
-  unsigned long long P = 0ull;  // fixed-point top-p mass target
-  if (has_p) {
-    const float t = fmaxf(rp.tp, 0.f) * S * 1099511627776.0f;
-    P = t >= 1.8e19f ? ~0ull : static_cast<unsigned long long>(t);
-  }
+  const unsigned long long P = bd.P;  // fixed-point top-p mass target
   int npass = 0;  // histogram parity
   // Largest key x >= key(lo) with count(>= x) >= k (top-k) or mass(>= x) >= P
   // (top-p), counting candidates of the tiles' buffers or of a re-read of the
@@ -1281,8 +1307,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
         if (d < 0) return;
         const bool leader = lane == __ffs(peers) - 1;
         if (has_p) {
-          const float e = ex2((x - lmax) * c2);
-          const unsigned long long mm = __float2ull_rn(e * 1099511627776.0f);
+          const unsigned long long mm = mass40(x, lmax, c2);
           const unsigned hi = __reduce_add_sync(peers, unsigned(mm >> 20));
           const unsigned lw = __reduce_add_sync(peers, unsigned(mm & 0xFFFFFu));
           if (leader)
@@ -1433,7 +1458,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
         const bool cand = ((cb >> e) & 1u) && x > -INFINITY;
         if (cand && x >= hi2) {
           ++ca;
-          ma += __float2ull_rn(ex2((x - lmax) * c2) * 1099511627776.0f);
+          ma += mass40(x, lmax, c2);
         }
         const bool in = cand && x >= lo2 && x < hi2;
         const unsigned bal = __ballot_sync(kFullWarp, in);
@@ -1475,13 +1500,45 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
     return descend(true, lo2, out_key, hi2, ca, ma);
   };
 
+  // At most one staged entry per thread: the threshold by counting.  Thread i
+  // sums the count and mass of the staged entries at or above its own logit;
+  // the threshold is the largest staged logit at which a target is reached --
+  // the radix descent's answer, since counts and masses change only at entries.
+  // False when no entry reaches a target.
+  auto select_few = [&](uint32_t& out_key) -> bool {
+    const bool mine = unsigned(tid) < nst;
+    const float xi = mine ? bval[tid] : 0.f;
+    if (has_p) hist.mass[0][tid] = mine ? mass40(xi, lmax, c2) : 0ull;
+    __syncthreads();
+    unsigned cnt = 0u;
+    unsigned long long ms = 0ull;
+    if (mine) {
+      for (unsigned j = 0; j < nst; ++j) {
+        if (bval[j] >= xi) {
+          ++cnt;
+          if (has_p) ms += hist.mass[0][j];
+        }
+      }
+    }
+    const bool hit = mine && ((has_k && cnt >= unsigned(k)) || (has_p && ms >= P));
+    const unsigned kk = __reduce_max_sync(kFullWarp, hit ? fkey(xi) : 0u);
+    if (lane == 0) scan_c[warp] = kk;
+    __syncthreads();
+    unsigned top = 0u;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) top = max(top, scan_c[w]);
+    __syncthreads();  // scan_c and hist are free again
+    out_key = top;
+    return top != 0u;
+  };
+
   float thr = fm;
   bool from_buffers = !any_overflow;
   if (has_k || has_p) {
     uint32_t kx = 0;
     bool found = false;
     if (from_buffers) {
-      found = descend(true, lo_b, kx);
+      found = staged && nst <= unsigned(kThreads) ? select_few(kx) : descend(true, lo_b, kx);
       if (!found && !(fm >= lo_b)) from_buffers = false;
     }
     if (!from_buffers) found = window_select(kx) || descend(false, fcut, kx);
