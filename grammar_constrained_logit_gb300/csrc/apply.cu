@@ -4,11 +4,12 @@
 // One streaming pass over the selected rows.  Each thread owns whole 16-byte
 // vectors of a row (4 float32 or 8 half/bfloat16 tokens) and reads the one or two
 // bitmask words that cover them (consecutive lanes share a word, so the warp's
-// mask read is one broadcast-coalesced sector).  In place, a vector whose tokens
-// are all kept is neither read nor written, and a vector whose tokens are all
-// masked is written with the fill pattern without being read; only mixed vectors
-// are read, blended and written back.  Out of place, every vector of every row is
-// written once (masked rows blended, other rows copied).
+// mask read is one broadcast-coalesced sector).  In place nothing is read but
+// the bitmask: a vector whose tokens are all kept is not touched, a vector whose
+// tokens are all masked is written with the fill pattern, and in a mixed vector
+// only the masked elements are written (element or element-pair stores).  Out of
+// place, every vector of every row is written once (masked rows blended, other
+// rows copied).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -46,6 +47,29 @@ __device__ __forceinline__ uint4 ld_stream(const char* p) {
 }
 __device__ __forceinline__ void st_stream(char* p, const uint4& v) {
   __stcs(reinterpret_cast<uint4*>(p), v);
+}
+
+// The fill pattern into the masked elements of one 16-byte vector (bit e of keep
+// set: element e kept and left alone).
+template <int DT>
+__device__ __forceinline__ void store_masked(char* p, uint32_t keep, uint32_t fill_w) {
+  if constexpr (DT == LP_F32) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (!((keep >> e) & 1u)) __stcs(reinterpret_cast<unsigned*>(p) + e, fill_w);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {  // element pair i is 32-bit word i
+      const uint32_t m = (~keep >> (2 * i)) & 3u;
+      if (m == 3u)
+        __stcs(reinterpret_cast<unsigned*>(p) + i, fill_w);
+      else if (m == 1u)
+        __stcs(reinterpret_cast<unsigned short*>(p) + 2 * i, static_cast<unsigned short>(fill_w));
+      else if (m == 2u)
+        __stcs(reinterpret_cast<unsigned short*>(p) + 2 * i + 1,
+               static_cast<unsigned short>(fill_w >> 16));
+    }
+  }
 }
 
 template <int DT, bool OOP>
@@ -121,10 +145,10 @@ __global__ void __launch_bounds__(kApplyThreads) apply_kernel(const ApplyArgs a)
          j += blockDim.x)
       scalar(j);
 
-    // whole vectors of this block's vector range: every mask word, then every
-    // logits vector that must be read, then the stores, so that one thread's
-    // loads are all in flight together (a store may alias a later load, which
-    // would otherwise hold that load back behind it)
+    // whole vectors of this block's vector range: every mask word, then (out of
+    // place) every logits vector that must be read, then the stores, so that one
+    // thread's loads are all in flight together (a store may alias a later load,
+    // which would otherwise hold that load back behind it)
     int64_t j0[kVecPerThread];
     uint32_t keep[kVecPerThread];
 #pragma unroll
@@ -134,15 +158,21 @@ __global__ void __launch_bounds__(kApplyThreads) apply_kernel(const ApplyArgs a)
       keep[k] = q >= nvec ? ~0u : sel ? mask_bits(mrow, j0[k], EPV, limit) : ALL;
     }
     uint4 v[kVecPerThread];
+    if (OOP) {
 #pragma unroll
-    for (int k = 0; k < kVecPerThread; ++k)
-      if (keep[k] != ~0u && keep[k] != 0u && (OOP || keep[k] != ALL))
-        v[k] = ld_stream(rin + j0[k] * EB);
+      for (int k = 0; k < kVecPerThread; ++k)
+        if (keep[k] != ~0u && keep[k] != 0u) v[k] = ld_stream(rin + j0[k] * EB);
+    }
 #pragma unroll
     for (int k = 0; k < kVecPerThread; ++k) {
       if (keep[k] == ~0u || (!OOP && keep[k] == ALL)) continue;
+      char* const dst = rout + j0[k] * EB;
+      if (!OOP && keep[k] != 0u) {
+        store_masked<DT>(dst, keep[k], fill_w);
+        continue;
+      }
       const uint4 w = keep[k] == 0u ? fill_v : keep[k] == ALL ? v[k] : E::blend(v[k], keep[k], a.fill);
-      st_stream(rout + j0[k] * EB, w);
+      st_stream(dst, w);
     }
   }
 }
