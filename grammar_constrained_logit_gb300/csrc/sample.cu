@@ -1271,6 +1271,9 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
 
   // ---------------------------------- radix select of the threshold
   const unsigned long long P = bd.P;  // fixed-point top-p mass target
+  // the selection targets (a sample's are scaled versions of the row's)
+  int sel_k = has_k ? k : 0;
+  unsigned long long sel_P = P;
   int npass = 0;  // histogram parity
   // Largest key x >= key(lo) with count(>= x) >= k (top-k) or mass(>= x) >= P
   // (top-p), counting candidates of the tiles' buffers or of a re-read of the
@@ -1353,7 +1356,8 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
       }
       const unsigned cc = above_c + sc;
       const unsigned long long cm = above_m + smass;
-      const bool okb = cc > 0u && ((has_k && cc >= unsigned(k)) || (has_p && cm >= P));
+      const bool okb =
+          cc > 0u && ((sel_k > 0 && cc >= unsigned(sel_k)) || (has_p && cm >= sel_P));
       if (okb) atomicMax(&s_sel, tid);
       __syncthreads();
       const int sel = s_sel;
@@ -1520,7 +1524,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
         }
       }
     }
-    const bool hit = mine && ((has_k && cnt >= unsigned(k)) || (has_p && ms >= P));
+    const bool hit = mine && ((sel_k > 0 && cnt >= unsigned(sel_k)) || (has_p && ms >= sel_P));
     const unsigned kk = __reduce_max_sync(kFullWarp, hit ? fkey(xi) : 0u);
     if (lane == 0) scan_c[warp] = kk;
     __syncthreads();
@@ -1532,6 +1536,148 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
     return top != 0u;
   };
 
+  // ---------------- a row read once more, narrowed by a sample (buffers missed)
+  // A strided sample of the row's vectors (kStage elements, a fraction fr of the
+  // row) stands in for the row.  Its own threshold for scaled targets is a likely
+  // lower bound b of the row's: for top-k a quarter more than k fr candidates;
+  // for top-p the sample's mass less half the row's tail budget (S - P) scaled
+  // by fr, so that the row's mass below b is likely within its budget.  When the
+  // sample says that the candidates at or above b would fit in shared memory, one
+  // pass over the row counts them and their mass exactly and stages them.  When
+  // they reach a target (so the row's threshold is at least b) and fit, the
+  // threshold is selected among them, and the draw takes them with no further
+  // pass.  False otherwise (nothing is decided from the sample alone).
+  auto sample_select = [&](uint32_t& out_key) -> bool {
+    if (!rw_ready) {
+      rw.init(a, row, 0, a.V, row_masked(a, row));
+      rw_ready = true;
+    }
+    constexpr int per = kStage / EPV;  // sampled vectors
+    if (rw.nvec < 4 * per) return false;
+    const int sv = rw.nvec / per;  // sample stride, in vectors
+    const double fr = double(per) / double(rw.nvec);  // the sampled fraction of the row
+    // 1. the sampled vectors' candidates at or above fcut, staged
+    if (tid == 0) s_nst = 0u;
+    __syncthreads();
+    for (int base = 0; base < per; base += kThreads) {
+      const int si = base + tid;
+      uint4 raw = make_uint4(0, 0, 0, 0);
+      uint32_t cb = 0;
+      int i0 = 0;
+      if (si < per) {
+        const int q = si * sv;
+        cb = rw.bits(q, i0, nullptr, 0, 0);
+        if (cb) raw = rw.gvec(q);
+      }
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        const float x = E::get(raw, e);
+        const bool in = ((cb >> e) & 1u) && x > -INFINITY && x >= fcut;
+        const unsigned bal = __ballot_sync(kFullWarp, in);
+        unsigned pos = 0u;
+        if (lane == 0 && bal) pos = atomicAdd(&s_nst, unsigned(__popc(bal)));
+        pos = __shfl_sync(kFullWarp, pos, 0) + unsigned(__popc(bal & ((1u << lane) - 1u)));
+        if (in && pos < unsigned(kStage)) {
+          bval[pos] = x;
+          bidx[pos] = rw.start + i0 + e;
+        }
+      }
+    }
+    __syncthreads();
+    nst = min(s_nst, unsigned(kStage));
+    __syncthreads();
+    if (nst == 0u) return false;
+    staged = true;
+    // 2. the sample's threshold for the scaled targets
+    unsigned long long mt = 0ull;  // the sample's mass
+    if (has_p) {
+      for (unsigned i = unsigned(tid); i < nst; i += kThreads) mt += mass40(bval[i], lmax, c2);
+#pragma unroll
+      for (int o = 16; o; o >>= 1) mt += __shfl_xor_sync(kFullWarp, mt, o);
+      if (lane == 0) scan_m[warp] = mt;
+      __syncthreads();
+      mt = 0ull;
+      for (int w = 0; w < kWarps; ++w) mt += scan_m[w];
+      __syncthreads();
+    }
+    const double budget = 0.5 * fr * (double(S) * 1099511627776.0 - double(P));
+    sel_k = has_k ? int(fmin(ceil(1.25 * double(k) * fr) + 8.0, 2.0e9)) : 0;
+    sel_P = has_p && double(mt) > budget ? static_cast<unsigned long long>(double(mt) - budget)
+                                         : 0ull;
+    uint32_t kb = 0;
+    const bool got = (!has_p || sel_P > 0ull) &&
+                     (nst <= unsigned(kThreads) ? select_few(kb) : descend(true, fcut, kb));
+    sel_k = has_k ? k : 0;
+    sel_P = P;
+    if (!got) {
+      staged = false;
+      return false;
+    }
+    const float bnd = fmaxf(key_float(kb), fcut);
+    // the sample's count at or above bnd, scaled: more than fits -> no pass
+    unsigned cs = 0u;
+    for (unsigned i = unsigned(tid); i < nst; i += kThreads) cs += bval[i] >= bnd ? 1u : 0u;
+    cs = __reduce_add_sync(kFullWarp, cs);
+    if (lane == 0) scan_c[warp] = cs;
+    __syncthreads();
+    cs = 0u;
+    for (int w = 0; w < kWarps; ++w) cs += scan_c[w];
+    __syncthreads();
+    staged = false;
+    if (double(cs) > 0.75 * double(kStage) * fr) return false;
+    // 3. one pass: exact count and mass at or above bnd, those candidates staged
+    unsigned ca = 0u;
+    unsigned long long ma = 0ull;
+    if (tid == 0) s_nst = 0u;
+    __syncthreads();
+    reread([&](const uint4& raw, uint32_t cb, int i0) {
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        const float x = E::get(raw, e);
+        const bool in = ((cb >> e) & 1u) && x > -INFINITY && x >= bnd;
+        if (in) {
+          ++ca;
+          if (has_p) ma += mass40(x, lmax, c2);
+        }
+        const unsigned bal = __ballot_sync(kFullWarp, in);
+        if (!bal) continue;
+        unsigned pos = 0u;
+        if (lane == 0) pos = atomicAdd(&s_nst, unsigned(__popc(bal)));
+        pos = __shfl_sync(kFullWarp, pos, 0) + unsigned(__popc(bal & ((1u << lane) - 1u)));
+        if (in && pos < unsigned(kStage)) {
+          bval[pos] = x;
+          bidx[pos] = rw.start + i0 + e;
+        }
+      }
+    });
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      ca += __shfl_xor_sync(kFullWarp, ca, o);
+      ma += __shfl_xor_sync(kFullWarp, ma, o);
+    }
+    if (lane == 0) {
+      scan_c[warp] = ca;
+      scan_m[warp] = ma;
+    }
+    __syncthreads();
+    ca = 0u;
+    ma = 0ull;
+    for (int w = 0; w < kWarps; ++w) {
+      ca += scan_c[w];
+      ma += scan_m[w];
+    }
+    const unsigned n = s_nst;
+    __syncthreads();
+    if (n > unsigned(kStage)) return false;                       // too many to stage
+    if (!((has_k && ca >= unsigned(k)) || (has_p && ma >= P))) return false;  // b too high
+    // 4. the threshold among them
+    nst = n;
+    staged = true;
+    if (nst <= unsigned(kThreads) ? select_few(out_key) : descend(true, bnd, out_key)) return true;
+    staged = false;
+    return false;
+  };
+
   float thr = fm;
   bool from_buffers = !any_overflow;
   if (has_k || has_p) {
@@ -1541,7 +1687,13 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
       found = staged && nst <= unsigned(kThreads) ? select_few(kx) : descend(true, lo_b, kx);
       if (!found && !(fm >= lo_b)) from_buffers = false;
     }
-    if (!from_buffers) found = window_select(kx) || descend(false, fcut, kx);
+    if (!from_buffers) {
+      found = sample_select(kx);
+      if (found)
+        from_buffers = true;  // every kept candidate is staged: the draw takes them
+      else
+        found = window_select(kx) || descend(false, fcut, kx);
+    }
     if (found) thr = fmaxf(key_float(kx), fm);
   } else if (from_buffers && !(fm >= lo_w)) {
     from_buffers = false;
