@@ -234,10 +234,28 @@ __device__ __forceinline__ void launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 
-struct Hist {  // radix histograms, double-buffered by pass parity
-  unsigned long long mass[2][256];
+// Radix histograms, double-buffered by pass parity.  A bin's mass (a sum of
+// 2^-40 fixed-point masses, each at most 2^40) is kept exactly in three 32-bit
+// limbs of 14, 14 and 13 bits per addend, since 64-bit shared-memory atomics are
+// far slower than 32-bit ones; a limb cannot overflow while a bin takes at most
+// kLimbRows addends per pass.  Rows with more candidates use 64-bit atomics.
+constexpr unsigned kLimbRows = 1u << 18;
+struct Hist {
+  union {
+    unsigned long long mass[2][256];
+    unsigned limb[2][256][3];
+  };
   unsigned cnt[2][256];
 };
+__device__ __forceinline__ void limb_add(unsigned* l, unsigned long long m) {
+  atomicAdd(l, unsigned(m & 0x3FFFu));
+  atomicAdd(l + 1, unsigned((m >> 14) & 0x3FFFu));
+  atomicAdd(l + 2, unsigned(m >> 28));
+}
+__device__ __forceinline__ unsigned long long limb_sum(const unsigned* l) {
+  return static_cast<unsigned long long>(l[0]) + (static_cast<unsigned long long>(l[1]) << 14) +
+         (static_cast<unsigned long long>(l[2]) << 28);
+}
 
 __device__ __forceinline__ void arg_combine(float& s, int& v, float s2, int v2) {
   if (s2 > s || (s2 == s && v2 < v)) {
@@ -1271,6 +1289,9 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
 
   // ---------------------------------- radix select of the threshold
   const unsigned long long P = bd.P;  // fixed-point top-p mass target
+  // a radix pass keeps its bins' masses in 32-bit limbs unless the row has more
+  // candidates than a limb can sum
+  const bool limbs = unsigned(ncand_ub) <= kLimbRows;
   // the selection targets (a sample's are scaled versions of the row's)
   int sel_k = has_k ? k : 0;
   unsigned long long sel_P = P;
@@ -1293,30 +1314,32 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
       const int hp = npass & 1;
       ++npass;
       hist.cnt[hp][tid] = 0u;
-      hist.mass[hp][tid] = 0ull;
+      if (limbs) {
+        hist.limb[hp][tid][0] = 0u;
+        hist.limb[hp][tid][1] = 0u;
+        hist.limb[hp][tid][2] = 0u;
+      } else {
+        hist.mass[hp][tid] = 0ull;
+      }
       if (tid == 0) s_sel = -1;
       __syncthreads();
       const uint32_t himask = top >= 32 ? 0u : ~((1u << top) - 1u);
       const uint32_t dmask = (1u << (top - shift)) - 1u;
-      // warp-uniform: every lane calls with its element (or part = false)
+      // element x (when part) into its bin: one 32-bit atomic for the count and,
+      // for top-p rows, three for the mass limbs (or one 64-bit atomic)
       auto add = [&](float x, bool part) {
-        int d = -1;
-        if (part && x >= lo) {
-          const uint32_t kx = fkey(x);
-          if (((kx ^ prefix) & himask) == 0u) d = int((kx >> shift) & dmask);
-        }
-        if (!__any_sync(kFullWarp, d >= 0)) return;
-        const unsigned peers = __match_any_sync(kFullWarp, d);
-        if (d < 0) return;
-        const bool leader = lane == __ffs(peers) - 1;
+        if (!(part && x >= lo)) return;
+        const uint32_t kx = fkey(x);
+        if (((kx ^ prefix) & himask) != 0u) return;
+        const int d = int((kx >> shift) & dmask);
         if (has_p) {
           const unsigned long long mm = mass40(x, lmax, c2);
-          const unsigned hi = __reduce_add_sync(peers, unsigned(mm >> 20));
-          const unsigned lw = __reduce_add_sync(peers, unsigned(mm & 0xFFFFFu));
-          if (leader)
-            atomicAdd(&hist.mass[hp][d], (static_cast<unsigned long long>(hi) << 20) + lw);
+          if (limbs)
+            limb_add(hist.limb[hp][d], mm);
+          else
+            atomicAdd(&hist.mass[hp][d], mm);
         }
-        if (leader) atomicAdd(&hist.cnt[hp][d], unsigned(__popc(peers)));
+        atomicAdd(&hist.cnt[hp][d], 1u);
       };
       if (from_buffers) {
         buffered([&](float x, int, bool ok) { add(x, ok); });
@@ -1333,7 +1356,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
       __syncthreads();
       // bin tid, then a descending inclusive scan over the bins
       const unsigned c = hist.cnt[hp][tid];
-      const unsigned long long mass = hist.mass[hp][tid];
+      const unsigned long long mass = limbs ? limb_sum(hist.limb[hp][tid]) : hist.mass[hp][tid];
       unsigned sc = c;
       unsigned long long smass = mass;
 #pragma unroll
