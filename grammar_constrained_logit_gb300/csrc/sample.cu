@@ -763,7 +763,7 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
             }
           }
         }
-        if constexpr (compact) {  // warp-uniform: append the piece's candidates within the window
+        if constexpr (compact) {  // append the piece's candidates within the window
           // the warp's running maximum as an order key (0: none yet), published to
           // the CTA when it rises
           const unsigned wk = __reduce_max_sync(kFullWarp, m > -INFINITY ? fkey(m) : 0u);
@@ -781,28 +781,19 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
           const float cut = rk ? __fsub_rd(key_float(rk), delta) : -INFINITY;
 #pragma unroll
           for (int r = 0; r < kPerPiece; ++r) {
-            // a lane without a vector has vms = -inf, which must not pass a cut of -inf
+            // a lane without a vector has vms = -inf, which must not pass a cut of -inf;
+            // few lanes are live once the cut has risen, so each takes its own
+            // places with one shared-memory atomic (no warp-wide scan)
             const bool live = vms[r] > -INFINITY && vms[r] >= cut;
-            if (!__any_sync(kFullWarp, live)) continue;
+            if (!live) continue;
             const int q = pm.x + r * kConsumers + tid;
             uint32_t pass = 0;
-            if (live) {
 #pragma unroll
-              for (int e = 0; e < EPV; ++e) {
-                const float x = E::get(mv[r], e);
-                if (x >= cut && x > -INFINITY) pass |= 1u << e;
-              }
+            for (int e = 0; e < EPV; ++e) {
+              const float x = E::get(mv[r], e);
+              if (x >= cut && x > -INFINITY) pass |= 1u << e;
             }
-            const int n = __popc(pass);
-            int incl = n;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-              const int y = __shfl_up_sync(kFullWarp, incl, o);
-              if (lane >= o) incl += y;
-            }
-            int pos = 0;
-            if (lane == 31) pos = atomicAdd(&s_count[par], incl);
-            pos = __shfl_sync(kFullWarp, pos, 31) + incl - n;
+            int pos = atomicAdd(&s_count[par], __popc(pass));
             const int i0 = (16 * q - pt.mis) / Sp::EB;
             while (pass) {
               const int e = __ffs(pass) - 1;
