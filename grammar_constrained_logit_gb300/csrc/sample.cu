@@ -624,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
     __syncwarp();
 
     // the largest running maximum the row's other tiles have published, read one
-    // piece ahead of its use (thread 0); the largest key this warp has published
+    // piece ahead of its use (thread 0); the largest key this lane has published
     unsigned hint = 0u, wpub = 0u;
 
     // ------------------------------------------------------ stream the tile
@@ -764,10 +764,10 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
           }
         }
         if constexpr (compact) {  // append the piece's candidates within the window
-          // the warp's running maximum as an order key (0: none yet), published to
-          // the CTA when it rises
-          const unsigned wk = __reduce_max_sync(kFullWarp, m > -INFINITY ? fkey(m) : 0u);
-          if (lane == 0 && wk > wpub) {
+          // this lane's running maximum as an order key (0: none yet), published
+          // to the CTA when it rises
+          const unsigned wk = m > -INFINITY ? fkey(m) : 0u;
+          if (wk > wpub) {
             atomicMax(&s_runkey[par], wk);
             wpub = wk;
           }
