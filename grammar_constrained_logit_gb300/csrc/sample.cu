@@ -225,6 +225,29 @@ __device__ __forceinline__ float gumbel_score(float z, int v, int row, uint64_t 
   return z + gumbel_from_word(word);
 }
 
+// The Gumbel score of candidate v if it may reach `best`, else -inf, without the
+// two logarithms for most tokens that cannot: with u the token's uniform,
+// g = -log(w) and w = -log(u) >= 1 - u, so 1 - u > e^(z - best) (taken with a
+// margin above the approximate exponential) proves z + g < best.  1 - u is exact
+// in float.  Used only where best is a score already seen, so a skipped token
+// can never be the draw.
+__device__ __forceinline__ float gumbel_score_vs(float z, int v, int row, uint64_t offset,
+                                                uint2 key, uint4& w4, int& wgrp, float best) {
+  const int grp = v >> 2;
+  if (grp != wgrp) {
+    w4 = philox4x32_10(
+        make_uint4(uint32_t(grp), uint32_t(row), uint32_t(offset), uint32_t(offset >> 32)), key);
+    wgrp = grp;
+  }
+  const uint32_t word = (v & 3) == 0 ? w4.x : (v & 3) == 1 ? w4.y : (v & 3) == 2 ? w4.z : w4.w;
+  if (best > -INFINITY) {
+    const float one_minus_u = (float(8388608u - (word >> 9)) - 0.5f) * 1.1920928955078125e-07f;
+    const float bound = ex2((z - best) * kLog2e) * 1.0001f;
+    if (one_minus_u > bound) return -INFINITY;
+  }
+  return z + gumbel_from_word(word);
+}
+
 // Programmatic dependent launch: wait for the grid this one depends on, and let
 // the next grid in the stream begin its launch.
 __device__ __forceinline__ void grid_dependency_wait() {
@@ -759,7 +782,8 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
               const float z = __fdiv_rn(x, T);
               if (z + kGumbelMax < best) continue;  // cannot win
               const int v = pt.start + i0 + e;
-              arg_combine(best, bestv, gumbel_score(z, v, row, a.offset, key, w4, wgrp), v);
+              arg_combine(best, bestv,
+                          gumbel_score_vs(z, v, row, a.offset, key, w4, wgrp, best), v);
             }
           }
         }
@@ -778,7 +802,11 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
             hint = *(volatile unsigned*)&a.rowkey[lrow];
           }
           const unsigned rk = max(wk, *(volatile unsigned*)&s_runkey[par]);
-          const float cut = rk ? __fsub_rd(key_float(rk), delta) : -INFINITY;
+          // a buffer that has overflowed is flagged at the tile's end whatever else
+          // is appended: stop appending
+          const float cut = *(volatile int*)&s_count[par] > kCapT ? INFINITY
+                            : rk                                   ? __fsub_rd(key_float(rk), delta)
+                                                                   : -INFINITY;
 #pragma unroll
           for (int r = 0; r < kPerPiece; ++r) {
             // a lane without a vector has vms = -inf, which must not pass a cut of -inf;
@@ -1734,7 +1762,8 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
         const float z = __fdiv_rn(x, T);
         if (z + kGumbelMax < best) continue;
         const int v = rw.start + i0 + e;
-        arg_combine(best, bestv, gumbel_score(z, v, row, a.offset, key, w4, wgrp), v);
+        arg_combine(best, bestv, gumbel_score_vs(z, v, row, a.offset, key, w4, wgrp, best),
+                    v);
       }
     });
   }
