@@ -8,10 +8,11 @@
 // Accelerator, in a persistent grid of three CTAs per SM.  Every row is cut into
 // tiles of equal length (8-64 KB of logits) and the CTAs take the tiles of all
 // rows round-robin, so the work per SM is even whatever the batch size and
-// vocabulary.  A CTA streams its tiles through a ring of four 7 KB
+// vocabulary.  A CTA streams its tiles through a ring of three 14 KB
 // shared-memory stages: a producer warp keeps bulk copies (cp.async.bulk, with
 // the stage's bitmask words) in flight on mbarriers, and seven consumer warps
-// take each landed stage from shared memory.  Per tile:
+// take each landed stage from shared memory, four 16-byte vectors per thread.
+// Per tile:
 //   * candidate max with its lowest index, the candidate count and, for top-p
 //     rows, an online softmax sum;
 //   * filtered rows: every candidate within a window below the tile's running
@@ -30,15 +31,16 @@
 // The finish kernel (one CTA per row, launched as a programmatic dependent of
 // the stream kernel so that its launch overlaps the stream) merges the row's
 // tile summaries: no candidate -> -1; greedy -> argmax; unfiltered -> the best
-// score's token.  Filtered rows find the keep-threshold max(t_k, t_p, t_m) by
-// an MSD radix select over the order-preserving key of the logit -- counts for
-// top-k and 2^-40 fixed-point softmax mass for top-p, pre-summed per warp
-// (match_any + redux); one descent serves both filters: the threshold is the
-// largest key at which "count >= k" or "mass >= top_p S" first holds.  The
-// descent reads the tiles' buffers (L2 resident), counting only the region where
-// they are complete; if the threshold is not there (or a buffer overflowed) the
-// CTA reads the whole row again and selects and draws from that.  The draw is
-// Gumbel-max over the kept set with Philox4x32-10 noise keyed by
+// score's token.  Filtered rows find the keep-threshold max(t_k, t_p, t_m) as
+// the largest logit at which "count >= k" or "mass >= top_p S" first holds
+// (counts for top-k, 2^-40 fixed-point softmax mass for top-p): by counting when
+// few candidates are staged, else by an MSD radix select over the
+// order-preserving key of the logit.  The selection reads the tiles' buffers (L2
+// resident), counting only the region where they are complete; if the threshold
+// is not there (or a buffer overflowed) the CTA reads the row again: a strided
+// sample bounds the threshold so that one pass can stage every candidate above
+// it, else a window search or the radix passes run over the re-read row.  The
+// draw is Gumbel-max over the kept set with Philox4x32-10 noise keyed by
 // (seed, row, offset).
 // Masses are integers, so every sum over tiles or warps is exact and
 // order-independent; softmax sums are merged in a fixed order.  Results are
