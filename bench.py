@@ -218,7 +218,7 @@ class Op:
     """One hot-path call on one workload, with a ring of device input copies."""
 
     def __init__(self, kind: str, w: syn.Workload, ring_bytes_min: int, torch, ops,
-                 min_copies: int = 2):
+                 min_copies: int = 2, row_flags: bool = False):
         self.kind, self.w, self.torch, self.ops = kind, w, torch, ops
         dev = torch.device("cuda")
         st = w.logits
@@ -241,6 +241,12 @@ class Op:
             b0 = torch.from_numpy(w.bitmask).to(dev)
             self.bitmask = [b0] + [b0.clone() for _ in range(self.R - 1)]
         self.indices = None if w.indices is None else torch.from_numpy(w.indices).to(dev)
+        # the per-row flag selector with its keeps-a-token report, in place of indices
+        self.flags = None
+        if row_flags and kind == "apply":
+            f = np.zeros(w.B, dtype=np.uint8)
+            f[np.arange(w.B) if w.indices is None else w.indices] = 1
+            self.flags = torch.from_numpy(f).to(dev)
         self.params = {k: torch.from_numpy(w.per_row(k)).to(dev)
                        for k in ("temperature", "top_k", "top_p", "min_p")}
         self.out = torch.empty(w.B, dtype=torch.int64, device=dev)
@@ -257,7 +263,9 @@ class Op:
         w, ops = self.w, self.ops
         lg = self.logits[slot % self.R][:, :w.cols]
         bm = None if self.bitmask is None else self.bitmask[slot % self.R]
-        if self.kind == "apply":
+        if self.kind == "apply" and self.flags is not None:
+            ops.apply_token_bitmask_rows(lg, bm, self.flags, vocab_size=w.vocab_size, report=True)
+        elif self.kind == "apply":
             ops.apply_token_bitmask_inplace(lg, bm, vocab_size=w.vocab_size, indices=self.indices)
         else:
             p = self.params
@@ -401,7 +409,8 @@ def run_gpu(args) -> dict | None:
         wa, wf = make_workload("apply_only"), make_workload("fused_sample")
         plan = [Op("apply", wa, ring_min, torch, ops, G), Op("sample", wf, ring_min, torch, ops)]
     elif args.workload == "apply_only":
-        plan = [Op("apply", make_workload("apply_only"), ring_min, torch, ops, G)]
+        plan = [Op("apply", make_workload("apply_only"), ring_min, torch, ops, G,
+                   row_flags=args.row_flags)]
     elif args.workload == "tiny_greedy":
         w = make_workload("tiny_greedy")
         plan = [Op("apply", w, ring_min, torch, ops), Op("sample", w, ring_min, torch, ops)]
@@ -474,6 +483,8 @@ def run_gpu(args) -> dict | None:
            "parallelism": f"replicas x{ws} (rows shard with no collective)"}
     for op in plan:
         cfg[f"ring_{op.kind}"] = op.R
+        if op.flags is not None:
+            cfg["selector"] = "per-row flags with the keeps-a-token report (lp_apply_token_bitmask_rows)"
     res["config"] = cfg
     lines = {}
     for op, t in zip(plan, per_op):
@@ -667,6 +678,9 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=90.0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--row-flags", action="store_true",
+                    help="apply_only: select the rows by per-row flags and report which keep a "
+                         "token (lp_apply_token_bitmask_rows) instead of indices")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     res = run_reference(args) if args.impl == "reference" else run_gpu(args)

@@ -35,6 +35,8 @@ struct ApplyArgs {
   int64_t bm_stride, bm_rows;
   const int32_t* indices;     // selected rows, or nullptr
   int64_t n_indices;
+  const uint8_t* row_flags;   // in place, no indices: row b masked iff row_flags[b] != 0
+  int32_t* has_token;         // in place: has_token[b] = 1 when row b keeps a token, else 0
   int64_t n_rows;             // row slots walked by blockIdx.y
   uint32_t fill;              // fill bit pattern of one element
   int use_bitmap;             // out of place with indices: selection bitmap in shared memory
@@ -109,7 +111,7 @@ __global__ void __launch_bounds__(kApplyThreads) apply_kernel(const ApplyArgs a)
     } else {
       b = a.indices ? int64_t(a.indices[slot]) : slot;
       if (b < 0 || b >= sel_limit) continue;  // invalid index: skipped
-      sel = true;
+      sel = a.row_flags == nullptr || a.row_flags[b] != 0;
     }
     const char* rin = a.in + b * a.in_stride;
     char* rout = OOP ? a.out + b * a.out_stride : const_cast<char*>(rin);
@@ -155,7 +157,14 @@ __global__ void __launch_bounds__(kApplyThreads) apply_kernel(const ApplyArgs a)
     for (int k = 0; k < kVecPerThread; ++k) {
       const int64_t q = int64_t(blockIdx.x) * kVecPerBlock + k * kApplyThreads + threadIdx.x;
       j0[k] = head + q * EPV;
-      keep[k] = q >= nvec ? ~0u : sel ? mask_bits(mrow, j0[k], EPV, limit) : ALL;
+      // with row flags the mask words load beside the flag, not after it
+      keep[k] = q >= nvec                        ? ~0u
+                : sel || a.row_flags != nullptr ? mask_bits(mrow, j0[k], EPV, a.vocab)
+                                                 : ALL;
+    }
+    if (!sel) {
+#pragma unroll
+      for (int k = 0; k < kVecPerThread; ++k) keep[k] = keep[k] == ~0u ? ~0u : ALL;
     }
     uint4 v[kVecPerThread];
     if (OOP) {
@@ -173,6 +182,21 @@ __global__ void __launch_bounds__(kApplyThreads) apply_kernel(const ApplyArgs a)
       }
       const uint4 w = keep[k] == 0u ? fill_v : keep[k] == ALL ? v[k] : E::blend(v[k], keep[k], a.fill);
       st_stream(dst, w);
+    }
+    // block-uniform: the row's first block reports the whole row (its words below
+    // vocab_size; an unflagged row keeps every token)
+    if (!OOP && a.has_token != nullptr && blockIdx.x == 0) {
+      bool kept = !sel && a.vocab > 0;
+      if (sel) {
+        const int64_t nw = (a.vocab + 31) >> 5;
+        for (int64_t w = threadIdx.x; w < nw; w += blockDim.x) {
+          uint32_t word = __ldg(mrow + w);
+          if (w == nw - 1 && (a.vocab & 31)) word &= (1u << (a.vocab & 31)) - 1u;
+          kept |= word != 0u;
+        }
+      }
+      const int r = __syncthreads_or(kept);
+      if (threadIdx.x == 0) a.has_token[b] = r ? 1 : 0;
     }
   }
 }
@@ -289,6 +313,44 @@ extern "C" lp_status lp_apply_token_bitmask(void* logits, lp_dtype dt, int64_t B
   a.indices = indices;
   a.n_indices = num_indices;
   a.n_rows = rows;
+  a.fill = fill_bits(-__builtin_huge_valf(), dt);
+  a.vec_ok = 1;
+  return launch_apply<false>(dt, a, g.vocab, stream) == cudaSuccess ? LP_OK : LP_ERR_CUDA;
+}
+
+extern "C" lp_status lp_apply_token_bitmask_rows(void* logits, lp_dtype dt, int64_t B,
+                                                 int64_t cols, int64_t logits_stride,
+                                                 const int32_t* bitmask, int64_t bitmask_rows,
+                                                 int64_t bitmask_words, int64_t bitmask_stride,
+                                                 int64_t vocab_size,
+                                                 const uint8_t* row_needs_mask,
+                                                 int32_t* row_has_token, cudaStream_t stream) {
+  Geometry g = check_common(dt, B, cols, logits_stride, bitmask_rows, bitmask_words,
+                            bitmask_stride, vocab_size, nullptr, 0);
+  if (g.status != LP_OK) return g.status;
+  if (B == 0) return LP_OK;
+  if (g.vocab > 0 && (logits == nullptr || bitmask == nullptr)) return LP_ERR_INVALID_ARGUMENT;
+  if (g.vocab == 0) {  // no row keeps a token, and there is nothing to mask
+    if (row_has_token != nullptr &&
+        cudaMemsetAsync(row_has_token, 0, size_t(B) * sizeof(int32_t), stream) != cudaSuccess)
+      return LP_ERR_CUDA;
+    return LP_OK;
+  }
+  const int64_t eb = elt_bytes(dt);
+  ApplyArgs a{};
+  a.out = static_cast<char*>(logits);
+  a.out_stride = logits_stride * eb;
+  a.in = static_cast<const char*>(logits);
+  a.in_stride = logits_stride * eb;
+  a.B = B;
+  a.cols = cols;
+  a.vocab = g.vocab;
+  a.bitmask = reinterpret_cast<const uint32_t*>(bitmask);
+  a.bm_stride = bitmask_stride;
+  a.bm_rows = bitmask_rows;
+  a.n_rows = B;
+  a.row_flags = row_needs_mask;
+  a.has_token = row_has_token;
   a.fill = fill_bits(-__builtin_huge_valf(), dt);
   a.vec_ok = 1;
   return launch_apply<false>(dt, a, g.vocab, stream) == cudaSuccess ? LP_OK : LP_ERR_CUDA;

@@ -103,6 +103,37 @@ def apply_token_bitmask_inplace(logits: torch.Tensor, bitmask: torch.Tensor, *,
 lp_apply_token_bitmask = apply_token_bitmask_inplace
 
 
+def apply_token_bitmask_rows(logits: torch.Tensor, bitmask: torch.Tensor,
+                             row_needs_mask: torch.Tensor | None = None, *,
+                             vocab_size: int | None = None,
+                             report: bool = False) -> torch.Tensor | None:
+    """Set masked logits to -inf in place in the rows whose ``row_needs_mask``
+    flag (uint8 or bool, one per row) is nonzero; every row when it is None.
+    With ``report``, returns int32 [B]: 1 where the row keeps a token after the
+    call, 0 where its mask admits none (an unsatisfiable row)."""
+    lg = _matrix(logits, "logits")
+    bm = _bitmask(bitmask, lg.device)
+    B = lg.size(0)
+    flags = None
+    if row_needs_mask is not None:
+        if row_needs_mask.device != lg.device:
+            raise ValueError("row_needs_mask must be on the same device as logits")
+        flags = row_needs_mask.to(torch.uint8).contiguous().view(-1)
+        if flags.numel() != B:
+            raise ValueError(f"row_needs_mask must have {B} entries")
+    has = torch.empty(B, dtype=torch.int32, device=lg.device) if report else None
+    lib = _lib.load()
+    st = lib.lp_apply_token_bitmask_rows(
+        _ptr(lg), _dtype_code(lg), B, lg.size(1), _stride(lg), _ptr(bm), bm.size(0), bm.size(1),
+        _stride(bm), -1 if vocab_size is None else int(vocab_size), _ptr(flags), _ptr(has),
+        _stream(lg))
+    check("lp_apply_token_bitmask_rows", st)
+    return has
+
+
+lp_apply_token_bitmask_rows = apply_token_bitmask_rows
+
+
 def apply_packed_bitmask(logits: torch.Tensor, bitmask: torch.Tensor,
                          fill_value: float = float("-inf"), *, out: torch.Tensor | None = None,
                          vocab_size: int | None = None,

@@ -4,6 +4,8 @@
  *
  * Operations (each entry point cites the page section that defines it):
  *   lp_apply_token_bitmask   in place, masked logits := -inf
+ *   lp_apply_token_bitmask_rows  the same with a per-row flag for the rows to
+ *                            mask, and an optional per-row "keeps a token" report
  *   lp_apply_packed_bitmask  out of place, masked logits := fill_value
  *   lp_sample                temperature, top-k ∩ top-p ∩ min-p, Gumbel-max draw
  *   lp_mask_and_sample       the bitmask applied on the fly, then lp_sample
@@ -97,6 +99,31 @@ lp_status lp_apply_token_bitmask(void* logits, lp_dtype dt, int64_t B, int64_t c
                                  int64_t bitmask_stride, int64_t vocab_size,
                                  const int32_t* indices, int64_t num_indices,
                                  cudaStream_t stream);
+
+/*
+ * lp_apply_token_bitmask_rows -- TensorRT-Edge-LLM "Guided Decoder": the mask the
+ * apply kernel reads comes with a per-row flag, and a row whose flag is zero is
+ * left alone (struct Impl, deviceRowNeedsMask); whether a row's mask admits a
+ * token (rowHasAnyToken) is what marks a slot unsatisfiable (fillMasks,
+ * unsatisfiableSlots).  Here both run on the device, in the apply's one pass.
+ *
+ * For each row b with row_needs_mask[b] != 0 (every row when row_needs_mask is
+ * NULL) and each token j < vocab_size whose bit is 0:
+ * logits[b * logits_stride + j] = -inf.  Nothing else changes.
+ *   row_needs_mask  device uint8 [B], or NULL
+ *   row_has_token   device int32 [B] written by the call, or NULL: 1 when row b
+ *                   keeps at least one token j < vocab_size after the call (an
+ *                   unflagged row keeps all of them), else 0; all zeros when
+ *                   vocab_size == 0.
+ * Other arguments, ownership and errors as lp_apply_token_bitmask without
+ * indices: bitmask_rows >= B is required.
+ */
+lp_status lp_apply_token_bitmask_rows(void* logits, lp_dtype dt, int64_t B, int64_t cols,
+                                      int64_t logits_stride, const int32_t* bitmask,
+                                      int64_t bitmask_rows, int64_t bitmask_words,
+                                      int64_t bitmask_stride, int64_t vocab_size,
+                                      const uint8_t* row_needs_mask, int32_t* row_has_token,
+                                      cudaStream_t stream);
 
 /*
  * lp_apply_packed_bitmask -- Modular MAX "apply_packed_bitmask": one fused pass,

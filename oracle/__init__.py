@@ -67,6 +67,8 @@ def load_library(path: str):
     lib.lpo_apply.restype = i32
     lib.lpo_apply.argtypes = [vp, i64, vp, i32, i64, i64, i64, vp, i64, i64, i64,
                               ctypes.c_float, i64, vp, i64]
+    lib.lpo_apply_rows.restype = i32
+    lib.lpo_apply_rows.argtypes = [vp, i32, i64, i64, i64, vp, i64, i64, i64, i64, vp, vp]
     lib.lpo_mask_and_sample.restype = i32
     lib.lpo_mask_and_sample.argtypes = [vp, i32, i64, i64, i64, vp, i64, i64, i64, i64,
                                         vp, i64, vp, vp, vp, vp, u64, u64, vp, vp, vp, vp, vp]
@@ -127,6 +129,25 @@ def apply(logits: np.ndarray, bitmask: np.ndarray, *, dtype: int, fill: float = 
     if rc != 0:
         raise ValueError("inconsistent geometry")
     return out
+
+
+def apply_rows(logits: np.ndarray, bitmask: np.ndarray, *, dtype: int, flags=None,
+               vocab_size=None, cols=None):
+    """In-place apply on the rows whose flag is nonzero (all rows for None), on a
+    copy of ``logits``; returns (masked copy, int32 per-row "keeps a token")."""
+    lib = _load()
+    out = np.ascontiguousarray(logits).copy()
+    bitmask = np.ascontiguousarray(bitmask, dtype=np.int32)
+    B, stride = out.shape
+    cols = stride if cols is None else cols
+    fl = None if flags is None else np.ascontiguousarray(flags, dtype=np.uint8)
+    has = np.zeros(B, dtype=np.int32)
+    rc = lib.lpo_apply_rows(_ptr(out), dtype, B, cols, stride, _ptr(bitmask), bitmask.shape[0],
+                            bitmask.shape[1], bitmask.shape[1],
+                            -1 if vocab_size is None else int(vocab_size), _ptr(fl), _ptr(has))
+    if rc != 0:
+        raise ValueError("inconsistent geometry")
+    return out, has
 
 
 def _per_row(x, B, dt):

@@ -212,6 +212,35 @@ int lpo_apply(void* out, int64_t out_stride, const void* logits, int dtype, int6
   return 0;
 }
 
+/* [TRT] Guided Decoder, struct Impl: the mask the apply kernel reads comes with a
+   per-row flag (deviceRowNeedsMask), and a row whose flag is zero is left alone;
+   rowHasAnyToken is true when the row's mask admits at least one token, and
+   fillMasks reports a slot whose mask is all zero as unsatisfiable.  In place:
+   for each row b with flags == NULL or flags[b] != 0 and each j < vocab_size
+   whose bit is 0, logits[b, j] = -inf.  has_token (when not NULL) gets, per row,
+   1 if some j < vocab_size is kept (every j of an unflagged row), else 0.
+   Returns 0, or -1 for an inconsistent geometry (bitmask_rows < B included). */
+int lpo_apply_rows(void* logits, int dtype, int64_t B, int64_t cols, int64_t logits_stride,
+                   const int32_t* bitmask, int64_t bitmask_rows, int64_t bitmask_words,
+                   int64_t bitmask_stride, int64_t vocab_size, const uint8_t* flags,
+                   int32_t* has_token) {
+  vocab_size = lpo_resolve_vocab(vocab_size, cols, bitmask_words);
+  if (vocab_size > cols || vocab_size > bitmask_words * 32 || bitmask_rows < B) return -1;
+  for (int64_t b = 0; b < B; ++b) {
+    const int masked = flags == NULL || flags[b] != 0;
+    int any = 0;
+    for (int64_t j = 0; j < vocab_size; ++j) {
+      if (!masked || lpo_bit(bitmask, bitmask_stride, b, j)) {
+        any = 1;
+      } else {
+        lpo_store_fill(logits, dtype, b * logits_stride + j, -INFINITY);
+      }
+    }
+    if (has_token) has_token[b] = any;
+  }
+  return 0;
+}
+
 /* ------------------------------------------------------------------ Philox */
 
 /* [PH] Philox-4x32 with 10 rounds.  One round multiplies words 0 and 2 of the

@@ -80,6 +80,35 @@ def test_apply_no_work_is_ok(lib, kw):
     assert _apply(lib, **kw) == _lib.LP_OK
 
 
+def _rows(lib, **kw):
+    a = dict(logits=FAKE, dt=2, B=4, cols=64, stride=64, bm=FAKE, bm_rows=4, words=2,
+             bm_stride=2, vocab=-1, flags=None, has=None)
+    a.update(kw)
+    return lib.lp_apply_token_bitmask_rows(a["logits"], a["dt"], a["B"], a["cols"], a["stride"],
+                                           a["bm"], a["bm_rows"], a["words"], a["bm_stride"],
+                                           a["vocab"], a["flags"], a["has"], None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(B=-1), dict(cols=-1), dict(stride=63), dict(words=-1), dict(bm_stride=1),
+    dict(vocab=65), dict(bm_rows=3), dict(logits=None), dict(bm=None),
+    dict(logits=None, has=FAKE), dict(bm=None, flags=FAKE, has=FAKE),
+])
+def test_apply_rows_rejects(lib, kw):
+    # every rejection happens before the report is zeroed: nothing is enqueued
+    assert _rows(lib, **kw) == _lib.LP_ERR_INVALID_ARGUMENT
+
+
+def test_apply_rows_unsupported_dtype(lib):
+    assert _rows(lib, dt=5) == _lib.LP_ERR_UNSUPPORTED_DTYPE
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(B=0, has=FAKE), dict(vocab=0),
+                                dict(vocab=0, logits=None, bm=None)])
+def test_apply_rows_no_work_is_ok(lib, kw):
+    assert _rows(lib, **kw) == _lib.LP_OK
+
+
 def _oop(lib, **kw):
     a = dict(out=ctypes.c_void_p(0x2000), out_stride=64, logits=FAKE, dt=0, B=4, cols=64,
              stride=64, bm=FAKE, bm_rows=4, words=2, bm_stride=2, fill=-1.0, vocab=-1,

@@ -157,6 +157,64 @@ def test_random_parity(dtype, inplace):
             assert np.array_equal(_bits(_host(view, dtype)), _bits(logits))  # input untouched
 
 
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_rows_parity(dtype):
+    """Per-row flags and the keeps-a-token report, bit-exact against the oracle;
+    some flagged rows have an all-zero mask (report 0), and the report buffer is
+    zeroed by the call whatever it held."""
+    rng = np.random.default_rng(2000 + DT[dtype])
+    for trial in range(30):
+        B, cols, vocab, words, bm, logits, _ = _random_case(rng, dtype)
+        bm = bm.copy()
+        bm_rows = bm.shape[0]
+        if B > 1:
+            bm[int(rng.integers(0, B))] = 0
+        flags = rng.integers(0, 2, size=B).astype(np.uint8) if trial % 3 else None
+        stride = logits.shape[1]
+        guard, shift = 64, int(rng.integers(0, 3))
+        base, view = _dev_view(logits, dtype, guard, shift)
+        want, want_has = oracle.apply_rows(logits, bm[:, :words], dtype=DT[dtype], flags=flags,
+                                           vocab_size=vocab, cols=cols)
+        fl = None if flags is None else torch.from_numpy(flags).cuda()
+        has = ops.apply_token_bitmask_rows(view[:, :cols], torch.from_numpy(bm).cuda()[:, :words],
+                                           fl, vocab_size=vocab, report=True)
+        got = _host(view, dtype)
+        assert np.array_equal(_bits(got), _bits(want)), (trial, dtype, B, cols, vocab)
+        assert has.cpu().numpy().tolist() == want_has.tolist(), (trial, dtype, B, cols, vocab)
+        _check_guard(base, dtype, guard, shift, B * stride)
+        assert bm_rows >= B
+
+
+def test_rows_report_overwrites_and_without_report():
+    x = torch.zeros(3, 100, device="cuda")
+    bm = torch.zeros(3, 4, dtype=torch.int32, device="cuda")
+    bm[2, 0] = 1
+    has = ops.apply_token_bitmask_rows(x, bm, torch.tensor([1, 0, 1], dtype=torch.uint8,
+                                                           device="cuda"), report=True)
+    assert has.cpu().tolist() == [0, 1, 1]
+    assert torch.isinf(x[0]).all() and not torch.isinf(x[1]).any()
+    assert x[2, 0] == 0 and torch.isinf(x[2, 1:]).all()
+    # no flags: every row is masked; no report
+    assert ops.apply_token_bitmask_rows(x, bm, None) is None
+    assert torch.isinf(x[1]).all() and x[2, 0] == 0
+
+
+def test_apply_only_workload_as_row_flags():
+    """The 32 indexed rows of the bf16 apply workload given as per-row flags: the
+    same logits as the indexed apply, and a report of every row."""
+    w = syn.apply_only()
+    flags = np.zeros(w.B, dtype=np.uint8)
+    flags[w.indices] = 1
+    want, want_has = oracle.apply_rows(w.logits, w.bitmask, dtype=oracle.BF16, flags=flags,
+                                       vocab_size=w.vocab_size, cols=w.cols)
+    x = torch.from_numpy(w.logits.view(np.int16)).cuda().view(torch.bfloat16)
+    has = ops.apply_token_bitmask_rows(x[:, :w.cols], torch.from_numpy(w.bitmask).cuda(),
+                                       torch.from_numpy(flags).cuda(), vocab_size=w.vocab_size,
+                                       report=True)
+    assert np.array_equal(_host(x, "bf16"), want)
+    assert has.cpu().numpy().tolist() == want_has.tolist()
+
+
 def test_empty_cases():
     x = torch.randn(3, 40, device="cuda")
     ref = x.clone()

@@ -449,3 +449,65 @@ def test_single_kept_token_ignores_noise():
         ids = oracle.mask_and_sample(x, dtype=oracle.F32, temperature=1.0, top_k=0,
                                      top_p=1.0, min_p=0.99, seed=off, offset=off)
         assert ids[0] == 1
+
+
+# ------------------------------------------------- per-row flags and report
+# TensorRT-Edge-LLM "Guided Decoder", struct Impl (deviceRowNeedsMask,
+# rowHasAnyToken) and fillMasks (unsatisfiableSlots).
+
+def test_apply_rows_hand_worked():
+    """Three rows of four tokens, vocab_size 3: row 0 flagged with bits 0 and 2
+    set, row 1 flagged with no bit set (unsatisfiable), row 2 not flagged with
+    no bit set (left alone, keeps everything); token 3 is past vocab_size in
+    every row and never changes."""
+    x = np.arange(12, dtype=np.float32).reshape(3, 4)
+    bm = np.array([[0b0101], [0], [0]], dtype=np.int32)
+    out, has = oracle.apply_rows(x, bm, dtype=oracle.F32, flags=[1, 1, 0], vocab_size=3)
+    ninf = -np.inf
+    want = np.array([[0, ninf, 2, 3], [ninf, ninf, ninf, 7], [8, 9, 10, 11]], dtype=np.float32)
+    assert np.array_equal(out, want)
+    assert has.tolist() == [1, 0, 1]
+
+
+def test_apply_rows_report_edges():
+    """A kept bit only at vocab_size (outside the vocabulary) does not count;
+    one at vocab_size - 1 does; vocab_size 0 keeps nothing anywhere; with no
+    flags every row is masked."""
+    x = np.zeros((2, 64), dtype=np.float32)
+    bm = np.zeros((2, 2), dtype=np.int32)
+    bm[0, 1] = 1 << 8          # token 40
+    bm[1, 1] = 1 << 7          # token 39
+    _, has = oracle.apply_rows(x, bm, dtype=oracle.F32, vocab_size=40)
+    assert has.tolist() == [0, 1]
+    _, has = oracle.apply_rows(x, bm, dtype=oracle.F32, flags=[0, 0], vocab_size=0)
+    assert has.tolist() == [0, 0]
+
+
+@pytest.mark.parametrize("dtype", [oracle.F32, oracle.F16])
+def test_apply_rows_against_numpy_and_indices(dtype):
+    """The masked rows equal numpy's own bit unpacking applied to the flagged
+    rows, the report equals numpy's any() over the unpacked bits, and the result
+    equals the indexed apply on the list of flagged rows."""
+    rng = np.random.default_rng(77)
+    npdt = np.float32 if dtype == oracle.F32 else np.float16
+    for _ in range(20):
+        B = int(rng.integers(1, 7))
+        cols = int(rng.integers(1, 200))
+        vocab = int(rng.integers(0, cols + 1))
+        words = (cols + 31) // 32
+        bm = rng.integers(0, 2**32, size=(B, words), dtype=np.uint64).astype(np.uint32)
+        if B > 1:
+            bm[1] = 0
+        bm = bm.view(np.int32)
+        flags = rng.integers(0, 2, size=B).astype(np.uint8)
+        x = rng.standard_normal((B, cols)).astype(npdt)
+        out, has = oracle.apply_rows(x, bm, dtype=dtype, flags=flags, vocab_size=vocab)
+        bits = np.unpackbits(bm.view(np.uint8), axis=1, bitorder="little")[:, :cols].astype(bool)
+        drop = (flags[:, None] != 0) & ~bits & (np.arange(cols)[None, :] < vocab)
+        want = np.where(drop, npdt(-np.inf), x)
+        assert np.array_equal(out.view(np.uint8), want.view(np.uint8))
+        keeps = ~drop & (np.arange(cols)[None, :] < vocab)
+        assert has.tolist() == keeps.any(axis=1).astype(int).tolist()
+        via_idx = oracle.apply(x, bm, dtype=dtype, vocab_size=vocab,
+                               indices=np.flatnonzero(flags).astype(np.int32))
+        assert np.array_equal(out.view(np.uint8), via_idx.view(np.uint8))
