@@ -19,7 +19,8 @@ LP_OK, LP_ERR_INVALID_ARGUMENT, LP_ERR_UNSUPPORTED_DTYPE, LP_ERR_CUDA, LP_ERR_TO
 
 EXPORTS = ("lp_apply_token_bitmask", "lp_apply_token_bitmask_rows", "lp_apply_packed_bitmask",
            "lp_sample",
-           "lp_mask_and_sample", "lp_sample_workspace_bytes", "lp_mask_and_sample_noalloc",
+           "lp_mask_and_sample", "lp_mask_and_sample_slots", "lp_sample_workspace_bytes",
+           "lp_mask_and_sample_noalloc",
            "lp_philox4x32_10", "lp_status_string")
 
 
@@ -61,6 +62,11 @@ def declare(lib) -> None:
     lib.lp_mask_and_sample.argtypes = [c_vp, c_i32, c_i64, c_i64, c_i64, c_vp, c_i64, c_i64,
                                        c_i64, c_i64, c_vp, c_i64, ctypes.POINTER(SamplingParams),
                                        c_vp, c_vp, c_i64, c_vp]
+    lib.lp_mask_and_sample_slots.restype = c_i32
+    lib.lp_mask_and_sample_slots.argtypes = [c_vp, c_i32, c_i64, c_i64, c_i64, c_vp, c_i64,
+                                             c_i64, c_i64, c_i64, c_vp, c_i64,
+                                             ctypes.POINTER(SamplingParams), c_i64, c_vp, c_vp,
+                                             c_vp, c_i64, c_vp]
     lib.lp_mask_and_sample_noalloc.restype = c_i32
     lib.lp_mask_and_sample_noalloc.argtypes = [c_vp, c_i32, c_i64, c_i64, c_i64, c_vp, c_i64,
                                                c_i64, c_i64, c_i64, c_vp, c_i64,

@@ -158,6 +158,8 @@ struct SampleArgs {
   const float* minp;
   float minp_s;
   uint64_t seed, offset;
+  int rps;                // rows per slot: row b takes the parameters at b / rps
+  const uint64_t* seeds;  // [rows] per-row Philox keys, or nullptr for seed
   int64_t* out;
   WsHeader* hdr;
   unsigned* rowkey;  // [rows]: largest published running maximum per row (order key; 0 none)
@@ -183,13 +185,20 @@ struct RawParams {
   float T, tp, mp;
   int k;
 };
+// Row `row`'s parameters: its slot's, rps rows to a slot.
 __device__ __forceinline__ RawParams raw_params(const SampleArgs& a, int row) {
   RawParams p;
-  p.T = a.temp ? a.temp[row] : a.temp_s;
-  p.k = a.topk ? a.topk[row] : a.topk_s;
-  p.tp = a.topp ? a.topp[row] : a.topp_s;
-  p.mp = a.minp ? a.minp[row] : a.minp_s;
+  const int s = row / a.rps;
+  p.T = a.temp ? a.temp[s] : a.temp_s;
+  p.k = a.topk ? a.topk[s] : a.topk_s;
+  p.tp = a.topp ? a.topp[s] : a.topp_s;
+  p.mp = a.minp ? a.minp[s] : a.minp_s;
   return p;
+}
+// Row `row`'s Philox key: its own seed, or the call's.
+__device__ __forceinline__ uint2 philox_key(const SampleArgs& a, int row) {
+  const uint64_t seed = a.seeds ? a.seeds[row] : a.seed;
+  return make_uint2(uint32_t(seed), uint32_t(seed >> 32));
 }
 __device__ __forceinline__ RowParams row_params(const RawParams& p) {
   RowParams r;
@@ -516,6 +525,7 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
   __shared__ uint4 keep_tab[256];  // 16-bit types: per-word keep masks of 8 element bits
   __shared__ int4 pmeta[kRing];    // per slot: vectors [x, y), staged mask words [z, w)
   __shared__ int pflag[kRing];     // per slot: bit 0 whole vectors only, bit 1 row masked
+  __shared__ uint2 pkey[kRing];    // per slot: the Philox key of the piece's row
 
   if (tid == 0) {
     s_err = 0;
@@ -568,6 +578,7 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
       }
       Sp g;
       g.init_tile(a, row, part_of(tile), masked);
+      const uint2 rkey = philox_key(a, row);
       for (int j = 0; j < g.npieces; ++j, ++issued) {
         const int slot = int(issued % kRing);
         if (issued >= uint32_t(kRing) &&
@@ -598,6 +609,7 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
         if (lane != 0) continue;
         pmeta[slot] = make_int4(q0, q1, base, w1);  // published by the arrive below
         pflag[slot] = (q0 >= g.qf0 && q1 <= g.qf1 ? 1 : 0) | (g.masked ? 2 : 0);
+        pkey[slot] = rkey;
         if (*(volatile int*)&s_err) {  // a copy went missing: start no more (rows report -2)
           mbar_expect_tx(&full[slot], 0);
           continue;
@@ -615,7 +627,6 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
   }
 
   // =============================================================== consumers
-  const uint2 key = make_uint2(uint32_t(a.seed), uint32_t(a.seed >> 32));
   uint32_t consumed = 0, lost = 0;
   RawParams nxt{};  // the next tile's row parameters, loaded a tile ahead
   if (tile_of(0) < ntiles) nxt = raw_params(a, row_of(tile_of(0)));
@@ -770,6 +781,7 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
           }
         }
         if constexpr (unfiltered) {
+          const uint2 key = pkey[slot];  // the row's Philox key, published with the piece
           // the element loop is not unrolled: each Gumbel score inlines a Philox
           // block, and one copy per vector keeps the kernel's code small
 #pragma unroll
@@ -1062,7 +1074,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
   const int lrow = blockIdx.x;
   const int row = a.row0 + lrow;
   if (tid == 0) a.rowkey[lrow] = 0u;  // the row's key back to zero for the next call
-  const uint2 key = make_uint2(uint32_t(a.seed), uint32_t(a.seed >> 32));
+  const uint2 key = philox_key(a, row);
   const RowParams rp = row_params(raw_params(a, row));
   const float T = rp.T, c2 = rp.c2;
   const bool has_p = rp.has_p;
@@ -1937,7 +1949,8 @@ lp_status run_sample(const void* logits, lp_dtype dt, int64_t B, int64_t vocab,
                      int64_t logits_stride, const int32_t* bitmask, int64_t bitmask_rows,
                      int64_t bitmask_stride, const int32_t* indices, int64_t num_indices,
                      const lp_sampling_params* params, int64_t* out_ids, void* workspace,
-                     int64_t workspace_bytes, cudaStream_t stream) {
+                     int64_t workspace_bytes, cudaStream_t stream, int64_t rows_per_slot = 1,
+                     const uint64_t* seeds = nullptr) {
   if (B == 0) return LP_OK;
   if (logits == nullptr && vocab > 0) return LP_ERR_INVALID_ARGUMENT;
   if (out_ids == nullptr || params == nullptr) return LP_ERR_INVALID_ARGUMENT;
@@ -1967,6 +1980,8 @@ lp_status run_sample(const void* logits, lp_dtype dt, int64_t B, int64_t vocab,
   a.minp_s = params->min_p_scalar;
   a.seed = params->seed;
   a.offset = params->offset;
+  a.rps = int(rows_per_slot);
+  a.seeds = seeds;
   a.out = out_ids;
   char* ws = static_cast<char*>(workspace);
   cudaError_t e;
@@ -1999,14 +2014,14 @@ extern "C" lp_status lp_sample(const void* logits, lp_dtype dt, int64_t B, int64
                     out_ids, workspace, workspace_bytes, stream);
 }
 
-extern "C" lp_status lp_mask_and_sample(const void* logits, lp_dtype dt, int64_t B, int64_t cols,
-                                        int64_t logits_stride, const int32_t* bitmask,
-                                        int64_t bitmask_rows, int64_t bitmask_words,
-                                        int64_t bitmask_stride, int64_t vocab_size,
-                                        const int32_t* indices, int64_t num_indices,
-                                        const lp_sampling_params* params, int64_t* out_ids,
-                                        void* workspace, int64_t workspace_bytes,
-                                        cudaStream_t stream) {
+namespace {
+lp_status mask_and_sample(const void* logits, lp_dtype dt, int64_t B, int64_t cols,
+                          int64_t logits_stride, const int32_t* bitmask, int64_t bitmask_rows,
+                          int64_t bitmask_words, int64_t bitmask_stride, int64_t vocab_size,
+                          const int32_t* indices, int64_t num_indices,
+                          const lp_sampling_params* params, int64_t* out_ids, void* workspace,
+                          int64_t workspace_bytes, cudaStream_t stream, int64_t rows_per_slot,
+                          const uint64_t* seeds) {
   if (!(dt == LP_F32 || dt == LP_F16 || dt == LP_BF16)) return LP_ERR_UNSUPPORTED_DTYPE;
   if (B < 0 || cols < 0 || logits_stride < cols || num_indices < 0 ||
       (num_indices > 0 && indices == nullptr))
@@ -2015,7 +2030,7 @@ extern "C" lp_status lp_mask_and_sample(const void* logits, lp_dtype dt, int64_t
     const int64_t vocab = vocab_size < 0 ? cols : vocab_size;
     if (vocab > cols) return LP_ERR_INVALID_ARGUMENT;
     return run_sample(logits, dt, B, vocab, logits_stride, nullptr, 0, 0, nullptr, 0, params,
-                      out_ids, workspace, workspace_bytes, stream);
+                      out_ids, workspace, workspace_bytes, stream, rows_per_slot, seeds);
   }
   if (bitmask_words < 0 || bitmask_stride < bitmask_words || bitmask_rows < 0)
     return LP_ERR_INVALID_ARGUMENT;
@@ -2026,7 +2041,38 @@ extern "C" lp_status lp_mask_and_sample(const void* logits, lp_dtype dt, int64_t
   const bool any_masked = indices == nullptr || num_indices > 0;
   return run_sample(logits, dt, B, vocab, logits_stride, any_masked ? bitmask : nullptr,
                     bitmask_rows, bitmask_stride, indices, num_indices, params, out_ids,
-                    workspace, workspace_bytes, stream);
+                    workspace, workspace_bytes, stream, rows_per_slot, seeds);
+}
+}  // namespace
+
+extern "C" lp_status lp_mask_and_sample(const void* logits, lp_dtype dt, int64_t B, int64_t cols,
+                                        int64_t logits_stride, const int32_t* bitmask,
+                                        int64_t bitmask_rows, int64_t bitmask_words,
+                                        int64_t bitmask_stride, int64_t vocab_size,
+                                        const int32_t* indices, int64_t num_indices,
+                                        const lp_sampling_params* params, int64_t* out_ids,
+                                        void* workspace, int64_t workspace_bytes,
+                                        cudaStream_t stream) {
+  return mask_and_sample(logits, dt, B, cols, logits_stride, bitmask, bitmask_rows,
+                         bitmask_words, bitmask_stride, vocab_size, indices, num_indices, params,
+                         out_ids, workspace, workspace_bytes, stream, 1, nullptr);
+}
+
+extern "C" lp_status lp_mask_and_sample_slots(const void* logits, lp_dtype dt, int64_t B,
+                                              int64_t cols, int64_t logits_stride,
+                                              const int32_t* bitmask, int64_t bitmask_rows,
+                                              int64_t bitmask_words, int64_t bitmask_stride,
+                                              int64_t vocab_size, const int32_t* indices,
+                                              int64_t num_indices,
+                                              const lp_sampling_params* params,
+                                              int64_t rows_per_slot, const uint64_t* seeds,
+                                              int64_t* out_ids, void* workspace,
+                                              int64_t workspace_bytes, cudaStream_t stream) {
+  if (rows_per_slot < 1 || rows_per_slot > 0x7fffffff || (B > 0 && B % rows_per_slot != 0))
+    return LP_ERR_INVALID_ARGUMENT;
+  return mask_and_sample(logits, dt, B, cols, logits_stride, bitmask, bitmask_rows,
+                         bitmask_words, bitmask_stride, vocab_size, indices, num_indices, params,
+                         out_ids, workspace, workspace_bytes, stream, rows_per_slot, seeds);
 }
 
 // Device scratch of the module itself, for callers that pass no workspace: zero

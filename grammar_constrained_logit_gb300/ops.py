@@ -278,6 +278,53 @@ def mask_and_sample(logits: torch.Tensor, bitmask: torch.Tensor | None, temperat
 lp_mask_and_sample = mask_and_sample
 
 
+def mask_and_sample_slots(logits: torch.Tensor, bitmask: torch.Tensor | None,
+                          rows_per_slot: int, temperature=1.0, top_k=0, top_p=1.0, min_p=0.0,
+                          seed: int = 0, offset: int = 0, *,
+                          seeds: torch.Tensor | None = None,
+                          indices: Sequence[int] | torch.Tensor | None = None,
+                          vocab_size: int | None = None,
+                          out: torch.Tensor | None = None,
+                          workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """``mask_and_sample`` on [slots, rows_per_slot, V] logits (or their
+    [slots * rows_per_slot, V] view): every sampling parameter is a scalar or
+    one value per slot, shared by the slot's rows; ``seeds`` (optional, one
+    uint64 per row, as int64 bit patterns) replaces ``seed`` row by row.
+    Returns int64 ids [slots * rows_per_slot]."""
+    if logits.dim() == 3:
+        if logits.size(1) != rows_per_slot:
+            raise ValueError("logits [slots, rows_per_slot, V] must match rows_per_slot")
+        logits = logits.reshape(-1, logits.size(2))
+    lg = _matrix(logits, "logits")
+    B = lg.size(0)
+    R = int(rows_per_slot)
+    if R < 1 or B % R:
+        raise ValueError("rows_per_slot must be >= 1 and divide the number of rows")
+    bm = None if bitmask is None else _bitmask(bitmask.reshape(-1, bitmask.size(-1)), lg.device)
+    idx = _indices(indices, lg.device)
+    keep: list = []
+    p = _params(B // R, lg.device, temperature, top_k, top_p, min_p, seed, offset, keep)
+    sd = None
+    if seeds is not None:
+        sd = seeds.to(device=lg.device, dtype=torch.int64).contiguous().view(-1)
+        if sd.numel() != B:
+            raise ValueError(f"seeds must have {B} entries")
+    ids = _ids_out(out, B, lg.device)
+    wp, wn = _workspace(workspace, lg, B, lg.size(1))
+    lib = _lib.load()
+    st = lib.lp_mask_and_sample_slots(
+        _ptr(lg), _dtype_code(lg), B, lg.size(1), _stride(lg), _ptr(bm),
+        0 if bm is None else bm.size(0), 0 if bm is None else bm.size(1),
+        0 if bm is None else _stride(bm), -1 if vocab_size is None else int(vocab_size),
+        _ptr(idx), 0 if idx is None else idx.numel(), ctypes.byref(p), R, _ptr(sd), _ptr(ids),
+        wp, wn, _stream(lg))
+    check("lp_mask_and_sample_slots", st)
+    return ids
+
+
+lp_mask_and_sample_slots = mask_and_sample_slots
+
+
 def philox4x32_10(counters: torch.Tensor, keys: torch.Tensor) -> torch.Tensor:
     """Device Philox4x32-10 on n blocks: counters [n, 4], keys [n, 2] (int32 bit
     patterns on the GPU) -> [n, 4] words (int32 bit patterns)."""

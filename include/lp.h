@@ -9,6 +9,8 @@
  *   lp_apply_packed_bitmask  out of place, masked logits := fill_value
  *   lp_sample                temperature, top-k ∩ top-p ∩ min-p, Gumbel-max draw
  *   lp_mask_and_sample       the bitmask applied on the fly, then lp_sample
+ *   lp_mask_and_sample_slots the same on [slots, rows_per_slot, V] logits with
+ *                            per-slot parameters and optional per-row seeds
  *
  * Common conventions
  *   - Logits are a row-major [B, cols] matrix of float32, float16 or bfloat16 with
@@ -208,6 +210,32 @@ lp_status lp_mask_and_sample(const void* logits, lp_dtype dt, int64_t B, int64_t
                              const int32_t* indices, int64_t num_indices,
                              const lp_sampling_params* params, int64_t* out_ids,
                              void* workspace, int64_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * lp_mask_and_sample_slots -- the speculative-verify layout of TensorRT-Edge-LLM
+ * "Guided Decoder" (applyMask: logits shaped [activeBatchSize, rowsPerSlot,
+ * vocab]; maxRowsPerSlot rows per slot), sampled as Kernel Hub
+ * "logits-processor", Ops, sample (per-row parameters; the draw keyed by
+ * (seed, row, offset)).
+ * lp_mask_and_sample on the B = slots * rows_per_slot rows of a
+ * [slots, rows_per_slot, cols] logits tensor (row b = slot * rows_per_slot + r),
+ * except that:
+ *   - every array in *params holds one value per SLOT (B / rows_per_slot of
+ *     them), and a slot's rows take its value;
+ *   - seeds, when not NULL, is a device uint64 [B]: row b draws with
+ *     (seeds[b], b, offset) instead of (params->seed, b, offset).
+ * rows_per_slot = 1 with seeds = NULL is lp_mask_and_sample.
+ * Invalid: rows_per_slot < 1, or B not a multiple of rows_per_slot; otherwise
+ * as lp_mask_and_sample.
+ */
+lp_status lp_mask_and_sample_slots(const void* logits, lp_dtype dt, int64_t B, int64_t cols,
+                                   int64_t logits_stride, const int32_t* bitmask,
+                                   int64_t bitmask_rows, int64_t bitmask_words,
+                                   int64_t bitmask_stride, int64_t vocab_size,
+                                   const int32_t* indices, int64_t num_indices,
+                                   const lp_sampling_params* params, int64_t rows_per_slot,
+                                   const uint64_t* seeds, int64_t* out_ids, void* workspace,
+                                   int64_t workspace_bytes, cudaStream_t stream);
 
 /*
  * lp_mask_and_sample_noalloc -- lp_mask_and_sample with no caller workspace: the

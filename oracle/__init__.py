@@ -161,14 +161,34 @@ def _per_row(x, B, dt):
 def mask_and_sample(logits: np.ndarray, *, dtype: int, bitmask=None, vocab_size=None,
                     indices=None, cols=None, temperature=1.0, top_k=0, top_p=1.0, min_p=0.0,
                     seed: int = 0, offset: int = 0, row_ids=None, want_keep: bool = False,
-                    want_p: bool = False, want_thr: bool = False):
+                    want_p: bool = False, want_thr: bool = False, seeds=None):
     """Per-row greedy / filtered Gumbel-max sampling (double precision).
 
     ``row_ids`` (optional, one per array row) gives each row's logical index,
     which keys the noise and addresses the bitmask (default 0..B-1), so a subset
     of a batch can be checked on its own.  Returns ids (int64 [B]) and, when
     asked, keep flags [B, V] (bool), probabilities [B, V] and thresholds [B] as a
-    tuple (ids, keep, p, thr)."""
+    tuple (ids, keep, p, thr).  ``seeds`` (optional, one per row) keys each row's
+    noise with its own seed: rows are independent, so each row is then sampled
+    on its own with its seed and its logical row index."""
+    if seeds is not None:
+        n = np.ascontiguousarray(logits).shape[0]
+        sd = [int(x) & (2**64 - 1) for x in np.asarray(seeds).astype(np.uint64).reshape(-1)]
+        assert len(sd) == n
+        rid = np.arange(n) if row_ids is None else np.asarray(row_ids)
+        parts = []
+        for b in range(n):
+            one = lambda x: x if np.ndim(x) == 0 else np.asarray(x)[b:b + 1]  # noqa: E731
+            parts.append(mask_and_sample(
+                np.ascontiguousarray(logits)[b:b + 1], dtype=dtype, bitmask=bitmask,
+                vocab_size=vocab_size, indices=indices, cols=cols,
+                temperature=one(temperature), top_k=one(top_k), top_p=one(top_p),
+                min_p=one(min_p), seed=sd[b], offset=offset, row_ids=rid[b:b + 1],
+                want_keep=want_keep, want_p=want_p, want_thr=want_thr))
+        if not (want_keep or want_p or want_thr):
+            return np.concatenate(parts)
+        cat = lambda k: None if parts[0][k] is None else np.concatenate([q[k] for q in parts])  # noqa: E731
+        return cat(0), cat(1), cat(2), cat(3)
     lib = _load()
     logits = np.ascontiguousarray(logits)
     B, stride = logits.shape

@@ -200,6 +200,21 @@ def test_mask_and_sample_validation(lib):
     assert call(wsn=16) == _lib.LP_ERR_INVALID_ARGUMENT
 
 
+def test_mask_and_sample_slots_validation(lib):
+    p = _params()
+    out = ctypes.c_void_p(0x3000)
+    call = lambda **kw: lib.lp_mask_and_sample_slots(  # noqa: E731
+        kw.get("logits", FAKE), 2, kw.get("B", 8), 64, 64, FAKE, 8, 2, 2, -1, None, 0,
+        ctypes.byref(p), kw.get("rps", 4), kw.get("seeds", None), out, kw.get("ws", WS),
+        kw.get("wsn", WSN), None)
+    assert call(rps=0) == _lib.LP_ERR_INVALID_ARGUMENT
+    assert call(rps=-2) == _lib.LP_ERR_INVALID_ARGUMENT
+    assert call(rps=3) == _lib.LP_ERR_INVALID_ARGUMENT   # 8 rows are not slots of 3
+    assert call(ws=None) == _lib.LP_ERR_INVALID_ARGUMENT
+    assert call(B=0) == _lib.LP_OK
+    assert call(B=0, rps=5) == _lib.LP_OK
+
+
 def test_philox_validation(lib):
     assert lib.lp_philox4x32_10(None, None, None, -1, None) == _lib.LP_ERR_INVALID_ARGUMENT
     assert lib.lp_philox4x32_10(None, None, None, 0, None) == _lib.LP_OK

@@ -423,6 +423,53 @@ def test_heterogeneous_rows_equal_broadcast():
 
 # ------------------------------------------------------ full-size workloads
 
+def test_slots_per_slot_params_and_row_seeds():
+    """The [slots, rows_per_slot, V] entry point: one parameter per slot shared by
+    its rows, and a Philox seed per row, against the oracle run with the slot
+    values repeated over the rows and the same seeds."""
+    R = 8
+    w = syn.speculative_verify(slots=12, rows_per_slot=R, V=20000, constrained_slots=6)
+    names = ("temperature", "top_k", "top_p", "min_p")
+    slot = {k: np.ascontiguousarray(w.per_row(k)[::R]) for k in names}
+    rowp = {k: np.repeat(v, R) for k, v in slot.items()}
+    seeds = np.random.default_rng(5).integers(0, 2**63, size=w.B, dtype=np.int64)
+    lg = to_dev(w.logits, w.dtype)[:, :w.cols]
+    bm = torch.from_numpy(w.bitmask).cuda()
+    idx = torch.from_numpy(w.indices).cuda()
+    p = {k: torch.from_numpy(v).cuda() for k, v in slot.items()}
+    g = ops.mask_and_sample_slots(lg, bm, R, p["temperature"], p["top_k"], p["top_p"],
+                                  p["min_p"], offset=3, seeds=torch.from_numpy(seeds).cuda(),
+                                  indices=idx, vocab_size=w.vocab_size).cpu().numpy()
+    common = dict(dtype=DT[w.dtype], bitmask=w.bitmask, vocab_size=w.vocab_size,
+                  indices=w.indices, cols=w.cols, offset=3, seeds=seeds.view(np.uint64),
+                  want_keep=True, want_p=True, want_thr=True)
+    ids, keep, pr, thr = oracle.mask_and_sample(w.logits, **rowp, **common)
+    tp = np.where(rowp["top_p"] < 1, np.minimum(rowp["top_p"] * (1 + REL),
+                                                 np.float32(0.99999994)), rowp["top_p"])
+    relaxed = dict(rowp, top_p=tp.astype(np.float32),
+                   min_p=(rowp["min_p"] * (1 - REL)).astype(np.float32))
+    _, keep2, _, _ = oracle.mask_and_sample(w.logits, **relaxed, **common)
+    for r in range(w.B):
+        v = int(g[r])
+        if ids[r] < 0 or thr[r] < 0:
+            assert v == ids[r], (r, v, ids[r])
+        else:
+            assert 0 <= v < keep.shape[1] and (keep[r, v] or keep2[r, v] or
+                                               pr[r, v] >= thr[r] * (1 - REL)), (r, v)
+    assert float(np.mean(g == ids)) >= 0.99
+    # one row per slot and no seeds: the plain entry point's ids
+    w1 = syn.speculative_verify(slots=6, rows_per_slot=4, V=5000, constrained_slots=3)
+    pp = {k: torch.from_numpy(w1.per_row(k)).cuda() for k in names}
+    l1 = to_dev(w1.logits, w1.dtype)[:, :w1.cols]
+    b1, i1 = torch.from_numpy(w1.bitmask).cuda(), torch.from_numpy(w1.indices).cuda()
+    a = ops.mask_and_sample(l1, b1, pp["temperature"], pp["top_k"], pp["top_p"], pp["min_p"],
+                            seed=11, offset=2, indices=i1, vocab_size=w1.vocab_size)
+    b = ops.mask_and_sample_slots(l1, b1, 1, pp["temperature"], pp["top_k"], pp["top_p"],
+                                  pp["min_p"], seed=11, offset=2, indices=i1,
+                                  vocab_size=w1.vocab_size)
+    assert torch.equal(a, b)
+
+
 def test_fused_sample_full_size():
     """B=256, V=131072 bf16, 10% mask, per-row T, top_k 50, top_p 0.9, min_p 0.05."""
     w = syn.fused_sample()

@@ -511,3 +511,25 @@ def test_apply_rows_against_numpy_and_indices(dtype):
         via_idx = oracle.apply(x, bm, dtype=dtype, vocab_size=vocab,
                                indices=np.flatnonzero(flags).astype(np.int32))
         assert np.array_equal(out.view(np.uint8), via_idx.view(np.uint8))
+
+
+# ------------------------------------------- per-row seeds and slot parameters
+# Kernel Hub "logits-processor", Ops, sample: the draw is keyed by (seed, row,
+# offset); TensorRT-Edge-LLM "Guided Decoder": rows grouped rowsPerSlot to a slot.
+
+def test_per_row_seeds_key_only_their_row():
+    """With every row's seed equal to the call's seed the draw is the scalar
+    seed's; a row's id depends on its own seed and not on the other rows'; and a
+    row keyed by seed s is the row the scalar seed s draws."""
+    rng = np.random.default_rng(9)
+    x = (rng.standard_normal((6, 500)) * 2).astype(np.float32)
+    kw = dict(dtype=oracle.F32, temperature=1.1, top_p=0.95)
+    base = oracle.mask_and_sample(x, seed=21, **kw)
+    assert np.array_equal(oracle.mask_and_sample(x, seeds=[21] * 6, **kw), base)
+    s1 = np.array([3, 4, 5, 6, 7, 8], dtype=np.uint64)
+    s2 = s1.copy()
+    s2[[0, 2, 5]] += 1000
+    a, b = oracle.mask_and_sample(x, seeds=s1, **kw), oracle.mask_and_sample(x, seeds=s2, **kw)
+    assert np.array_equal(a[[1, 3, 4]], b[[1, 3, 4]])
+    for r in range(6):
+        assert a[r] == oracle.mask_and_sample(x, seed=int(s1[r]), **kw)[r]
