@@ -18,6 +18,7 @@ LP_F32, LP_F16, LP_BF16 = 0, 1, 2
 LP_OK, LP_ERR_INVALID_ARGUMENT, LP_ERR_UNSUPPORTED_DTYPE, LP_ERR_CUDA, LP_ERR_TOO_LARGE = range(5)
 
 EXPORTS = ("lp_apply_token_bitmask", "lp_apply_token_bitmask_rows", "lp_apply_packed_bitmask",
+           "lp_upload_bitmask",
            "lp_sample",
            "lp_mask_and_sample", "lp_mask_and_sample_slots", "lp_sample_workspace_bytes",
            "lp_mask_and_sample_noalloc",
@@ -52,6 +53,9 @@ def declare(lib) -> None:
     lib.lp_apply_token_bitmask_rows.restype = c_i32
     lib.lp_apply_token_bitmask_rows.argtypes = [c_vp, c_i32, c_i64, c_i64, c_i64, c_vp, c_i64,
                                                 c_i64, c_i64, c_i64, c_vp, c_vp, c_vp]
+    lib.lp_upload_bitmask.restype = c_i32
+    lib.lp_upload_bitmask.argtypes = [c_vp, c_i64, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_vp,
+                                      c_vp]
     lib.lp_apply_packed_bitmask.restype = c_i32
     lib.lp_apply_packed_bitmask.argtypes = [c_vp, c_i64, c_vp, c_i32, c_i64, c_i64, c_i64, c_vp,
                                             c_i64, c_i64, c_i64, c_f32, c_i64, c_vp, c_i64, c_vp]

@@ -39,6 +39,12 @@ def _matrix(t: torch.Tensor, name: str) -> torch.Tensor:
     return t
 
 
+def _matrix_host(t: torch.Tensor) -> torch.Tensor:
+    if t.dim() != 2 or (t.size(1) > 1 and t.stride(1) != 1):
+        raise ValueError("host bitmask must be 2-D with contiguous rows")
+    return t
+
+
 def _stream(t: torch.Tensor):
     return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
 
@@ -132,6 +138,96 @@ def apply_token_bitmask_rows(logits: torch.Tensor, bitmask: torch.Tensor,
 
 
 lp_apply_token_bitmask_rows = apply_token_bitmask_rows
+
+
+def upload_bitmask(device_bitmask: torch.Tensor, host_bitmask: torch.Tensor, *,
+                   device_flags: torch.Tensor | None = None,
+                   host_flags: torch.Tensor | None = None,
+                   copy_stream: torch.cuda.Stream | None = None,
+                   event: torch.cuda.Event | None = None) -> torch.cuda.Event:
+    """Copy a host-filled bitmask (int32 [rows, words], best page-locked) and,
+    optionally, its uint8 row flags into device buffers on ``copy_stream`` (the
+    current stream when None), then record ``event`` (a new one when None) after
+    the copies and return it.  A compute stream waits on the event before an
+    apply reads the mask; the host must not touch the host buffers until the
+    event has completed."""
+    if host_bitmask.is_cuda or not device_bitmask.is_cuda:
+        raise ValueError("host_bitmask must be on the CPU and device_bitmask on the GPU")
+    hb, db = _matrix_host(host_bitmask), _matrix(device_bitmask, "device_bitmask")
+    if hb.dtype != torch.int32 or db.dtype != torch.int32:
+        raise TypeError("bitmasks must be int32")
+    rows, words = hb.size(0), hb.size(1)
+    if db.size(0) < rows or db.size(1) < words:
+        raise ValueError("device_bitmask is smaller than host_bitmask")
+    if (device_flags is None) != (host_flags is None):
+        raise ValueError("pass both row-flag buffers or neither")
+    if host_flags is not None and (host_flags.numel() < rows or device_flags.numel() < rows or
+                                   host_flags.dtype != torch.uint8 or
+                                   device_flags.dtype != torch.uint8):
+        raise ValueError("row flags must be uint8 with at least one entry per row")
+    stream = copy_stream if copy_stream is not None else torch.cuda.current_stream(db.device)
+    ev = event if event is not None else torch.cuda.Event()
+    lib = _lib.load()
+    # PyTorch creates an event's CUDA handle at its first record, so the event is
+    # recorded here, on the copy stream right after the enqueued copies
+    st = lib.lp_upload_bitmask(_ptr(db), _stride(db), _ptr(hb), _stride(hb), rows, words,
+                               _ptr(device_flags), _ptr(host_flags),
+                               ctypes.c_void_p(stream.cuda_stream), None)
+    check("lp_upload_bitmask", st)
+    ev.record(stream)
+    return ev
+
+
+lp_upload_bitmask = upload_bitmask
+
+
+class BitmaskStager:
+    """Double-buffered page-locked staging of the bitmask and its row flags.
+
+    Each step: ``host()`` gives the host buffers to fill (after the upload that
+    last used them has completed); ``upload()`` copies them to a device buffer
+    on a copy stream and makes the current stream wait for that copy, returning
+    the device buffers for the apply; ``consumed()`` marks, on the current
+    stream, that the apply enqueued after ``upload`` is done with them, so that
+    the copy two steps later may overwrite them."""
+
+    def __init__(self, rows: int, words: int, device=None):
+        dev = torch.device("cuda") if device is None else torch.device(device)
+        self.rows, self.words = rows, words
+        self.host_mask = [torch.zeros(rows, words, dtype=torch.int32).pin_memory()
+                          for _ in range(2)]
+        self.host_flags = [torch.zeros(rows, dtype=torch.uint8).pin_memory() for _ in range(2)]
+        self.dev_mask = [torch.zeros(rows, words, dtype=torch.int32, device=dev) for _ in range(2)]
+        self.dev_flags = [torch.zeros(rows, dtype=torch.uint8, device=dev) for _ in range(2)]
+        self.copy_stream = torch.cuda.Stream(device=dev)
+        self.uploaded = [None, None]
+        self.released = [None, None]
+        self.i = 0
+
+    def host(self):
+        """The host mask and flags of this step, free to fill."""
+        if self.uploaded[self.i] is not None:
+            self.uploaded[self.i].synchronize()
+        return self.host_mask[self.i], self.host_flags[self.i]
+
+    def upload(self):
+        """Start this step's copy; the current stream waits for it.  Returns the
+        device (mask, flags) the apply should read."""
+        i = self.i
+        if self.released[i] is not None:
+            self.copy_stream.wait_event(self.released[i])
+        ev = upload_bitmask(self.dev_mask[i], self.host_mask[i], device_flags=self.dev_flags[i],
+                            host_flags=self.host_flags[i], copy_stream=self.copy_stream)
+        self.uploaded[i] = ev
+        torch.cuda.current_stream(self.dev_mask[i].device).wait_event(ev)
+        return self.dev_mask[i], self.dev_flags[i]
+
+    def consumed(self):
+        """After enqueueing the apply: its device buffers may be reused later."""
+        ev = torch.cuda.Event()
+        ev.record(torch.cuda.current_stream(self.dev_mask[self.i].device))
+        self.released[self.i] = ev
+        self.i ^= 1
 
 
 def apply_packed_bitmask(logits: torch.Tensor, bitmask: torch.Tensor,

@@ -7,6 +7,8 @@
  *   lp_apply_token_bitmask_rows  the same with a per-row flag for the rows to
  *                            mask, and an optional per-row "keeps a token" report
  *   lp_apply_packed_bitmask  out of place, masked logits := fill_value
+ *   lp_upload_bitmask        a host-filled bitmask (and row flags) to the device on
+ *                            a copy stream, signalled by an event
  *   lp_sample                temperature, top-k ∩ top-p ∩ min-p, Gumbel-max draw
  *   lp_mask_and_sample       the bitmask applied on the fly, then lp_sample
  *   lp_mask_and_sample_slots the same on [slots, rows_per_slot, V] logits with
@@ -126,6 +128,33 @@ lp_status lp_apply_token_bitmask_rows(void* logits, lp_dtype dt, int64_t B, int6
                                       int64_t bitmask_stride, int64_t vocab_size,
                                       const uint8_t* row_needs_mask, int32_t* row_has_token,
                                       cudaStream_t stream);
+
+/*
+ * lp_upload_bitmask -- XGrammar "Bitmask Operations", Device: the bitmask is
+ * allocated on the CPU and must be copied to the GPU before the apply;
+ * TensorRT-Edge-LLM "Guided Decoder", struct Impl: hostBitmask and
+ * hostRowNeedsMask stage what the apply kernel reads from deviceBitmask and
+ * deviceRowNeedsMask, and captureDraftChains records an event instead of
+ * synchronising the stream.
+ *
+ * Enqueues on copy_stream the copy of rows [0, rows) x words [0, words) of the
+ * host bitmask (host_stride words per row) to the device bitmask (device_stride
+ * words per row), then, when both are given, of host_flags[0, rows) to
+ * device_flags; then records `uploaded` (when not NULL) on copy_stream.  A
+ * compute stream that waits on `uploaded` (cudaStreamWaitEvent) sees the new
+ * mask, and the copy overlaps whatever else the device runs.  Host buffers must
+ * stay untouched until `uploaded` completes, and should be page-locked for the
+ * copy to be asynchronous.  No kernel is launched.
+ *   device_bitmask  device int32, rows x device_stride words
+ *   host_bitmask    host int32, rows x host_stride words
+ *   device_flags / host_flags  uint8 [rows], both or neither
+ * Invalid: rows < 0, words < 0, a stride < words, only one of the two flag
+ * pointers, NULL bitmask pointers with rows > 0 and words > 0.
+ */
+lp_status lp_upload_bitmask(int32_t* device_bitmask, int64_t device_stride,
+                            const int32_t* host_bitmask, int64_t host_stride, int64_t rows,
+                            int64_t words, uint8_t* device_flags, const uint8_t* host_flags,
+                            cudaStream_t copy_stream, cudaEvent_t uploaded);
 
 /*
  * lp_apply_packed_bitmask -- Modular MAX "apply_packed_bitmask": one fused pass,

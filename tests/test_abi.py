@@ -200,6 +200,26 @@ def test_mask_and_sample_validation(lib):
     assert call(wsn=16) == _lib.LP_ERR_INVALID_ARGUMENT
 
 
+def _upload(lib, **kw):
+    a = dict(dev=FAKE, dstride=4, host=FAKE, hstride=4, rows=3, words=4, dflags=None,
+             hflags=None)
+    a.update(kw)
+    return lib.lp_upload_bitmask(a["dev"], a["dstride"], a["host"], a["hstride"], a["rows"],
+                                 a["words"], a["dflags"], a["hflags"], None, None)
+
+
+@pytest.mark.parametrize("kw", [dict(rows=-1), dict(words=-1), dict(dstride=3), dict(hstride=2),
+                                dict(dflags=FAKE), dict(hflags=FAKE), dict(dev=None),
+                                dict(host=None)])
+def test_upload_rejects(lib, kw):
+    assert _upload(lib, **kw) == _lib.LP_ERR_INVALID_ARGUMENT
+
+
+@pytest.mark.parametrize("kw", [dict(rows=0), dict(words=0, dev=None, host=None)])
+def test_upload_no_work_is_ok(lib, kw):
+    assert _upload(lib, **kw) == _lib.LP_OK
+
+
 def test_mask_and_sample_slots_validation(lib):
     p = _params()
     out = ctypes.c_void_p(0x3000)

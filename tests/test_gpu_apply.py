@@ -215,6 +215,51 @@ def test_apply_only_workload_as_row_flags():
     assert has.cpu().numpy().tolist() == want_has.tolist()
 
 
+def test_upload_then_apply_on_another_stream():
+    """A host-filled mask and row flags, copied on a side stream and signalled by
+    an event: the apply on the current stream, after waiting on the event, masks
+    exactly as the oracle does with the host mask."""
+    rng = np.random.default_rng(31)
+    B, cols = 16, 5000
+    words = (cols + 31) // 32
+    x = (rng.standard_normal((B, cols)) * 2).astype(np.float32)
+    hm = torch.from_numpy(rng.integers(0, 2**32, size=(B, words), dtype=np.uint64)
+                          .astype(np.uint32).view(np.int32)).pin_memory()
+    hf = torch.from_numpy((rng.random(B) < 0.5).astype(np.uint8)).pin_memory()
+    dm = torch.zeros(B, words + 3, dtype=torch.int32, device="cuda")[:, :words]
+    dfl = torch.zeros(B, dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+    ev = ops.upload_bitmask(dm, hm, device_flags=dfl, host_flags=hf, copy_stream=side)
+    torch.cuda.current_stream().wait_event(ev)
+    xd = torch.from_numpy(x).cuda()
+    has = ops.apply_token_bitmask_rows(xd, dm, dfl, report=True)
+    want, want_has = oracle.apply_rows(x, hm.numpy(), dtype=oracle.F32, flags=hf.numpy())
+    assert np.array_equal(xd.cpu().numpy().view(np.uint32), want.view(np.uint32))
+    assert has.cpu().numpy().tolist() == want_has.tolist()
+
+
+def test_bitmask_stager_steps():
+    """Five steps through the double-buffered stager, each with a new mask and new
+    flags filled on the host: every apply sees its own step's mask."""
+    rng = np.random.default_rng(32)
+    B, cols = 8, 3000
+    words = (cols + 31) // 32
+    st = ops.BitmaskStager(B, words)
+    for step in range(5):
+        hm, hf = st.host()
+        m = rng.integers(0, 2**32, size=(B, words), dtype=np.uint64).astype(np.uint32)
+        f = (rng.random(B) < 0.6).astype(np.uint8)
+        hm.copy_(torch.from_numpy(m.view(np.int32)))
+        hf.copy_(torch.from_numpy(f))
+        dm, dfl = st.upload()
+        x = (rng.standard_normal((B, cols))).astype(np.float32)
+        xd = torch.from_numpy(x).cuda()
+        ops.apply_token_bitmask_rows(xd, dm, dfl)
+        st.consumed()
+        want, _ = oracle.apply_rows(x, m.view(np.int32), dtype=oracle.F32, flags=f)
+        assert np.array_equal(xd.cpu().numpy().view(np.uint32), want.view(np.uint32)), step
+
+
 def test_empty_cases():
     x = torch.randn(3, 40, device="cuda")
     ref = x.clone()
