@@ -53,6 +53,15 @@ MUTANTS = [
      ["test_draw_is_exponential_race"]),
     ("unsat_not_minus_one", "*id_out = -1;\n    return 0;", "*id_out = 0;\n    return 0;",
      ["test_golden_greedy"]),
+    ("rows_flags_ignored", "const int masked = flags == NULL || flags[b] != 0;",
+     "const int masked = 1;",
+     ["test_apply_rows_hand_worked", "test_apply_rows_against_numpy_and_indices"]),
+    ("rows_unflagged_report_zero", "if (has_token) has_token[b] = any;",
+     "if (has_token) has_token[b] = masked ? any : 0;",
+     ["test_apply_rows_hand_worked", "test_apply_rows_against_numpy_and_indices"]),
+    ("rows_fill_sign", "lpo_store_fill(logits, dtype, b * logits_stride + j, -INFINITY);",
+     "lpo_store_fill(logits, dtype, b * logits_stride + j, INFINITY);",
+     ["test_apply_rows_hand_worked", "test_apply_rows_against_numpy_and_indices"]),
 ]
 
 
