@@ -258,6 +258,9 @@ class Op:
                                   dtype=torch.uint8, device=dev)
         self.bytes = touched
         self.units = w.B
+        # kernels one call launches: the apply kernel; or the sampler's stream and
+        # finish kernels per launch of at most 16384 rows
+        self.kernels = 1 if kind == "apply" else 2 * -(-w.B // 16384)
 
     def launch(self, slot: int, step: int):
         w, ops = self.w, self.ops
@@ -474,7 +477,7 @@ def run_gpu(args) -> dict | None:
            "ms_per_step": round(total_s / K * 1e3, 5), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": plan[0].w.dtype,
            "data": "synthetic (seeded generators shaped like the pages' workloads)",
-           "gpu_launches": K * len(plan) * ws}
+           "gpu_launches": K * sum(op.kernels for op in plan) * ws}
     cfg = {"workload": " + ".join(describe(op.w) for op in plan),
            "l2": f"an untimed write of 2x the {l2 >> 20} MB L2 before every graph replay, and "
                  "inputs in device rings (>= 4x the L2; an apply's copies do not repeat within "
