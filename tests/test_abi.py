@@ -32,6 +32,30 @@ def _declared():
     return names
 
 
+def test_header_is_plain_c(tmp_path):
+    """include/lp.h is a C header: a C99 file that includes it and names its types
+    compiles with the system C compiler (no C++ in the interface)."""
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    if cc is None or not os.path.isdir(cuda_inc):
+        pytest.skip("no C compiler or CUDA headers")
+    src = tmp_path / "use_lp.c"
+    src.write_text('#include "lp.h"\n'
+                   "int main(void) {\n"
+                   "  lp_sampling_params p = {0};\n"
+                   "  lp_dtype d = LP_BF16;\n"
+                   "  (void)p; (void)d;\n"
+                   "  return (int)LP_OK;\n"
+                   "}\n")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-fsyntax-only",
+                        f"-I{os.path.join(ROOT, 'include')}", f"-I{cuda_inc}", str(src)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
 def test_header_declares_the_entry_points():
     assert set(_lib.EXPORTS) <= _declared()
 
