@@ -1063,6 +1063,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
   __shared__ unsigned scan_c[kWarps];
   __shared__ unsigned long long scan_m[kWarps];
   __shared__ int s_sel, s_i[4];
+  __shared__ unsigned s_pub;  // the row's published key, as the stream kernel left it
   __shared__ float s_f[2];
   __shared__ unsigned s_above_c, s_total, s_nst;
   __shared__ unsigned long long s_above_m;
@@ -1073,7 +1074,10 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
 
   const int lrow = blockIdx.x;
   const int row = a.row0 + lrow;
-  if (tid == 0) a.rowkey[lrow] = 0u;  // the row's key back to zero for the next call
+  if (tid == 0) {  // the row's key, then back to zero for the next call
+    s_pub = a.rowkey[lrow];
+    a.rowkey[lrow] = 0u;
+  }
   const uint2 key = philox_key(a, row);
   const RowParams rp = row_params(raw_params(a, row));
   const float T = rp.T, c2 = rp.c2;
@@ -1187,7 +1191,10 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
   const float S = s_f[1];
   const int ncand_ub = s_i[1];  // candidates counted by their bits (-inf included)
   const bool row_err = (s_i[3] >> 1) != 0;
-  const bool any_overflow = (s_i[3] & 1) != 0;
+  // A published key above the row's maximum can only be stale (a workspace whose
+  // front was not zero when the call began): the cuts it raised may have dropped
+  // candidates, so the row is read again as if a buffer had overflowed.
+  const bool any_overflow = (s_i[3] & 1) != 0 || s_pub > (lmax > -INFINITY ? fkey(lmax) : 0u);
   const unsigned total = s_total;
 
   if (row_err || lmax == -INFINITY || rp.greedy || rp.unfiltered) {
@@ -1862,11 +1869,14 @@ WsPlan ws_plan(lp_dtype dt, int64_t B, int64_t V) {
   const int eb = elt_bytes(dt);
   const int64_t tpr_max = tiles_per_row(kTileBytesMin / eb, V);
   p.rows = std::max<int64_t>(1, std::min({B, kMaxRowsPerLaunch, kMaxTileSums / tpr_max}));
-  // full launches, and the last, shorter one (whose tiles may be shorter)
-  p.tiles = p.rows * tiles_per_row(tile_tokens(eb, p.rows, V), V);
-  const int64_t last = B % p.rows;
-  if (last) p.tiles = std::max(p.tiles, last * tiles_per_row(tile_tokens(eb, last, V), V));
-  p.pool = std::min(std::max(p.rows * kPoolPerRow, kPoolMin), kPoolMax);
+  // Tiles of one launch: at most nrows * ceil(V / longest tile) when the longest
+  // tile already gives kTileTarget tiles; else tile_tokens halved the tile from
+  // a length that gave fewer than kTileTarget, so at most 2 (kTileTarget - 1).
+  // The bound (and the pool) grow with B and V, so a workspace sized for one
+  // shape serves every smaller one.
+  const int64_t rows_cap = std::min(B, kMaxRowsPerLaunch);
+  p.tiles = std::max(2 * (kTileTarget - 1), rows_cap * tiles_per_row(kTileBytesMax / eb, V));
+  p.pool = std::min(std::max(rows_cap * kPoolPerRow, kPoolMin), kPoolMax);
   // The header and the per-row keys must be zero when a call starts; they sit
   // in a region of fixed size at the front, which no call of any shape uses for
   // anything else, and every call leaves them zero.
@@ -1928,6 +1938,7 @@ cudaError_t launch_sample(SampleArgs a, const WsPlan& plan, int64_t B, char* ws,
     a.chunk = int(tile);
     a.tpr = int(tiles_per_row(tile, a.V));
     a.ntiles = nr * a.tpr;
+    if (a.ntiles > plan.tiles) return cudaErrorInvalidValue;  // the plan bounds every launch
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(std::min<int64_t>(a.ntiles, G)));
     cfg.blockDim = dim3(kThreads);
@@ -2075,12 +2086,37 @@ extern "C" lp_status lp_mask_and_sample_slots(const void* logits, lp_dtype dt, i
                          out_ids, workspace, workspace_bytes, stream, rows_per_slot, seeds);
 }
 
-// Device scratch of the module itself, for callers that pass no workspace: zero
-// when the module loads (the state lp_sample needs), and kept so by every call.
+// Device scratch of the module itself, for callers that cannot allocate a
+// workspace: zero when the module loads (the state the sampler needs), and kept
+// so by every call.  Every device that loads the library holds it until exit.
 namespace lp {
 namespace {
 constexpr int64_t kNoAllocBytes = int64_t(128) << 20;
 __device__ __align__(256) unsigned char g_noalloc_ws[kNoAllocBytes];
+
+// The array's device address on the current device, looked up once per device
+// (the first call on a device does it) and then reused.
+constexpr int kMaxDevices = 64;
+void* noalloc_scratch(lp_status& st) {
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    st = LP_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_ws) != cudaSuccess) {
+      (void)cudaGetLastError();
+      st = LP_ERR_CUDA;
+      return nullptr;
+    }
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
 }  // namespace
 }  // namespace lp
 
@@ -2093,12 +2129,19 @@ extern "C" lp_status lp_mask_and_sample_noalloc(const void* logits, lp_dtype dt,
                                                 const lp_sampling_params* params,
                                                 int64_t* out_ids, cudaStream_t stream) {
   if (!(dt == LP_F32 || dt == LP_F16 || dt == LP_BF16)) return LP_ERR_UNSUPPORTED_DTYPE;
-  if (B < 0 || cols < 0) return LP_ERR_INVALID_ARGUMENT;
+  if (B < 0 || cols < 0 || bitmask_words < 0) return LP_ERR_INVALID_ARGUMENT;
   if (B == 0) return LP_OK;
-  // the widest vocabulary the call can use sizes the scratch it needs
-  if (lp_sample_workspace_bytes(dt, B, cols) > kNoAllocBytes) return LP_ERR_TOO_LARGE;
-  void* ws = nullptr;
-  if (cudaGetSymbolAddress(&ws, g_noalloc_ws) != cudaSuccess) return LP_ERR_CUDA;
+  // the vocabulary the call resolves to (as lp_mask_and_sample resolves it) sizes
+  // the scratch; an inconsistent one is refused by that entry point below
+  int64_t vocab = vocab_size >= 0 ? vocab_size
+                  : bitmask != nullptr ? std::min(cols, bitmask_words * 32)
+                                       : cols;
+  vocab = std::min(std::max<int64_t>(vocab, 0), cols);
+  const int64_t need = lp_sample_workspace_bytes(dt, B, vocab);
+  if (need < 0 || need > kNoAllocBytes) return LP_ERR_TOO_LARGE;
+  lp_status st = LP_OK;
+  void* ws = noalloc_scratch(st);
+  if (ws == nullptr) return st;
   return lp_mask_and_sample(logits, dt, B, cols, logits_stride, bitmask, bitmask_rows,
                             bitmask_words, bitmask_stride, vocab_size, indices, num_indices,
                             params, out_ids, ws, kNoAllocBytes, stream);
@@ -2120,7 +2163,9 @@ extern "C" const char* lp_status_string(lp_status status) {
     case LP_ERR_INVALID_ARGUMENT: return "invalid argument";
     case LP_ERR_UNSUPPORTED_DTYPE: return "unsupported dtype";
     case LP_ERR_CUDA: return "CUDA launch failed";
-    case LP_ERR_TOO_LARGE: return "size past the kernels' 32-bit index range";
+    case LP_ERR_TOO_LARGE:
+      return "size too large: past the kernels' 32-bit index range, or (noalloc) past the "
+             "library's fixed device scratch";
     default: return "unknown status";
   }
 }

@@ -29,9 +29,13 @@
  *     [0, min(B, bitmask_rows)) is skipped on the device: no access, no write.
  *     Indices should be unique; a duplicate gives the same result as one entry.
  *   - Pointers are DEVICE pointers unless stated otherwise.  The caller owns every
- *     buffer.  The library allocates no memory, keeps no state between calls,
- *     never synchronises, and only enqueues work on the given stream; a call is
- *     safe from several host threads at once on different buffers.
+ *     buffer.  No call allocates memory, and the library keeps no state between
+ *     calls beyond one fixed array: the 128 MiB device scratch of
+ *     lp_mask_and_sample_noalloc, which the CUDA module reserves (zero-filled) on
+ *     every device that loads it, whether or not that entry point is called, and
+ *     holds until the process exits.  Calls never synchronise and only enqueue
+ *     work on the given stream; a call is safe from several host threads at once
+ *     on different buffers.
  *   - Errors: arguments are checked on the host before any launch.  An invalid
  *     argument returns LP_ERR_INVALID_ARGUMENT and launches nothing.  A zero-size
  *     problem returns LP_OK and launches nothing.  A launch failure returns
@@ -54,7 +58,8 @@ typedef enum {
   LP_ERR_INVALID_ARGUMENT = 1,
   LP_ERR_UNSUPPORTED_DTYPE = 2,
   LP_ERR_CUDA = 3,
-  LP_ERR_TOO_LARGE = 4 /* a size past the 32-bit index range of the kernels */
+  LP_ERR_TOO_LARGE = 4 /* a size past the 32-bit index range of the kernels, or (noalloc)
+                          a call needing more scratch than the library's fixed array */
 } lp_status;
 
 /*
@@ -195,16 +200,26 @@ lp_status lp_apply_packed_bitmask(void* out, int64_t out_stride, const void* log
  *   params         host pointer, see lp_sampling_params
  *   workspace      device scratch of at least lp_sample_workspace_bytes(dt, B,
  *                  vocab_size) bytes, 256-byte aligned, owned by the caller.  It
- *                  must be zero-filled before its first use; after that the
- *                  library keeps it valid itself (every call leaves the counters
- *                  at its front zero), so one allocation serves any number of
- *                  calls of the same or smaller size.  Calls that share a workspace must
+ *                  should be zero-filled before its first use; after that the
+ *                  library keeps it valid itself (every call that completes
+ *                  leaves the counters in its first 256 + 4 * 16384 bytes zero),
+ *                  so one allocation serves any number of calls of the same or
+ *                  smaller size.  Results never depend on those counters: after a
+ *                  call that failed part-way (LP_ERR_CUDA after the first kernel
+ *                  was queued), or on a workspace that was not zero-filled, a
+ *                  call still returns correct ids -- a stale row key or pool
+ *                  counter only makes rows take the slower re-read path -- and
+ *                  resets the counters of the rows it samples.  To restore full
+ *                  speed at once, zero those first 256 + 4 * 16384 bytes again
+ *                  (or the whole workspace).  Calls that share a workspace must
  *                  be ordered (one stream, or events).  A NULL, misaligned or
  *                  short workspace is LP_ERR_INVALID_ARGUMENT.
  * Each call is two kernels on the stream: a streaming pass over the logits and
  * a per-row finish, the second launched as a programmatic dependent of the
- * first.  An id of -2 means a copy into shared memory did not complete within
- * the kernel's bounded wait (no such case is known).
+ * first.  An id of -2 means a wait inside the streaming kernel gave up (a copy
+ * into shared memory, or the hand-over of a tile's shared state, did not
+ * complete within its bounded wait; no such case is known); the call still
+ * completes and leaves the workspace valid.
  * Logits are read only.  vocab_size up to 2^31 - 65 and B up to 2^27 are
  * supported; larger sizes return LP_ERR_TOO_LARGE.
  */
@@ -267,15 +282,27 @@ lp_status lp_mask_and_sample_slots(const void* logits, lp_dtype dt, int64_t B, i
                                    int64_t workspace_bytes, cudaStream_t stream);
 
 /*
- * lp_mask_and_sample_noalloc -- lp_mask_and_sample with no caller workspace: the
- * call uses a 128 MiB device array that the library itself holds (allocated and
- * zero-filled when the library's module loads).  The pages have no counterpart;
- * it exists for callers that cannot allocate scratch.  Arguments, results and
- * errors as lp_mask_and_sample, plus LP_ERR_TOO_LARGE when
- * lp_sample_workspace_bytes(dt, B, cols) exceeds 128 MiB.  All calls of a
- * process share the one array, so they must be ordered (one stream, or
- * events): two such calls in flight at once on different streams are invalid
- * and not detected.
+ * lp_mask_and_sample_noalloc -- lp_mask_and_sample for callers that cannot
+ * allocate device memory themselves: code that must not call cudaMalloc (a
+ * caching allocator owns the device, or the call happens where allocation is
+ * not allowed, such as inside a captured region) and has no workspace to hand
+ * in.  The pages have no counterpart.  Instead of a caller workspace the call
+ * uses a 128 MiB device array of the library's own (a file-scope __device__
+ * array, zero-filled when the module loads and held by every device that loads
+ * the library until the process exits); it allocates nothing.
+ *   - Set-up: the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current and keeps it; make that
+ *     first call before any stream capture.
+ *   - Size: the scratch needed, lp_sample_workspace_bytes(dt, B, vocab) for the
+ *     vocabulary the call resolves to, must fit in 128 MiB; otherwise the call
+ *     returns LP_ERR_TOO_LARGE and launches nothing.  All five benchmark
+ *     workloads fit (the largest, 1024 rows of 202048 fp16 tokens, uses about
+ *     78 MiB).
+ *   - Sharing: every call uses the same array and leaves its counters zero for
+ *     the next.  Calls that overlap on the GPU (in flight at once on different
+ *     streams, or from several host threads without ordering) race on it and
+ *     give undefined ids; order them (one stream, or events).
+ * Arguments, results and other errors as lp_mask_and_sample.
  */
 lp_status lp_mask_and_sample_noalloc(const void* logits, lp_dtype dt, int64_t B, int64_t cols,
                                      int64_t logits_stride, const int32_t* bitmask,

@@ -199,6 +199,16 @@ def test_workspace_bytes(lib):
         sizes = [f(dt, B, V) for B, V in ((1, 1003), (64, 128256), (256, 131072), (1024, 202048))]
         assert all(n > 0 and n % 256 == 0 for n in sizes)
         assert sizes == sorted(sizes)  # more rows or tokens never need less
+    # monotone on a fine grid of shapes (tile halving rounds up, so a naive plan
+    # could need more scratch for a narrower vocabulary, e.g. 98304 vs 131072)
+    Bs = (1, 3, 64, 255, 256, 1000, 1024, 5000, 16384, 40000)
+    Vs = (1, 33, 1003, 8192, 32000, 65536, 98304, 100000, 131072, 202048, 262144, 1 << 20)
+    for dt in (0, 1, 2):
+        grid = [[f(dt, B, V) for V in Vs] for B in Bs]
+        for row in grid:
+            assert row == sorted(row)
+        for col in zip(*grid):
+            assert list(col) == sorted(col)
     # bounded: tile summaries and slots are a few percent of the logits, the pool
     # at most 128 MB
     for dt, eb in ((0, 4), (2, 2)):

@@ -32,32 +32,60 @@ def test_noalloc_refuses_oversized_calls():
 
 @pytest.mark.gpu
 def test_noalloc_matches_workspace_entry_point():
+    """Two rounds of calls of several shapes (an explicit vocab_size below the row
+    width, an index list of masked rows, three dtypes): every id equals the one
+    lp_mask_and_sample gives with a caller workspace, and is accepted by the
+    oracle's tolerance rule.  The shared array's counters are left zero by each
+    call (the same kernels keep a caller workspace's front zero, which the
+    workspace-reuse parity test reads back)."""
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from grammar_constrained_logit_gb300 import ops
     from grammar_constrained_logit_gb300 import synthetic as syn
+    from parity_check import check_ids
 
     lib = _lib.load()
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     rng = np.random.default_rng(12)
-    shapes = [(64, 20000, torch.bfloat16, True), (300, 5000, torch.float32, False),
-              (7, 70000, torch.float16, True), (64, 20000, torch.bfloat16, True)]
-    for it, (B, V, dt, masked) in enumerate(shapes):
-        x = torch.from_numpy((rng.standard_normal((B, V)) * 2).astype(np.float32)).cuda().to(dt)
-        bm = None
-        if masked:
-            allowed = rng.random((B, V)) < 0.3
-            bm = torch.from_numpy(syn.pack_bits(allowed)).cuda()
-        want = ops.mask_and_sample(x, bm, 0.8, 30, 0.9, 0.02, seed=5, offset=it)
-        got = torch.empty(B, dtype=torch.int64, device="cuda")
-        p = _params(offset=it)
-        st = lib.lp_mask_and_sample_noalloc(
-            ctypes.c_void_p(x.data_ptr()), {torch.float32: 0, torch.float16: 1,
-                                            torch.bfloat16: 2}[dt], B, V, V,
-            ctypes.c_void_p(0 if bm is None else bm.data_ptr()),
-            0 if bm is None else bm.size(0), 0 if bm is None else bm.size(1),
-            0 if bm is None else bm.size(1), -1, None, 0, ctypes.byref(p),
-            ctypes.c_void_p(got.data_ptr()), stream)
-        assert st == _lib.LP_OK
-        assert torch.equal(got, want), it
+    code = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+    name = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}
+    # (B, cols, dtype, masked, vocab_size or None, number of indexed rows or None)
+    shapes = [(64, 20000, torch.bfloat16, True, None, None),
+              (300, 5000, torch.float32, False, None, None),
+              (7, 70000, torch.float16, True, None, None),
+              (40, 9000, torch.float32, True, 8700, None),
+              (48, 12000, torch.bfloat16, True, None, 20)]
+    for rnd in range(2):
+        for it, (B, V, dt, masked, vocab, nidx) in enumerate(shapes):
+            off = 10 * rnd + it
+            x32 = (rng.standard_normal((B, V)) * 2).astype(np.float32)
+            x = torch.from_numpy(x32).cuda().to(dt)
+            bm = idx = None
+            bm_np = idx_np = None
+            if masked:
+                bm_np = syn.pack_bits(rng.random((B, V)) < 0.3)
+                bm = torch.from_numpy(bm_np).cuda()
+            if nidx is not None:
+                idx_np = np.sort(rng.choice(B, size=nidx, replace=False)).astype(np.int32)
+                idx = torch.from_numpy(idx_np).cuda()
+            want = ops.mask_and_sample(x, bm, 0.8, 30, 0.9, 0.02, seed=5, offset=off,
+                                       indices=idx, vocab_size=vocab)
+            got = torch.empty(B, dtype=torch.int64, device="cuda")
+            p = _params(offset=off)
+            st = lib.lp_mask_and_sample_noalloc(
+                ctypes.c_void_p(x.data_ptr()), code[dt], B, V, V,
+                ctypes.c_void_p(0 if bm is None else bm.data_ptr()),
+                0 if bm is None else bm.size(0), 0 if bm is None else bm.size(1),
+                0 if bm is None else bm.size(1), -1 if vocab is None else vocab,
+                ctypes.c_void_p(0 if idx is None else idx.data_ptr()),
+                0 if idx is None else idx.numel(), ctypes.byref(p),
+                ctypes.c_void_p(got.data_ptr()), stream)
+            assert st == _lib.LP_OK
+            assert torch.equal(got, want), (rnd, it)
+            # the oracle's rule on the same inputs (bf16 compared on its bit patterns)
+            st_np = syn.to_storage(x32, name[dt]) if dt != torch.float32 else x32
+            prm = {"temperature": np.full(B, 0.8, np.float32), "top_k": np.full(B, 30, np.int32),
+                   "top_p": np.full(B, 0.9, np.float32), "min_p": np.full(B, 0.02, np.float32)}
+            check_ids(st_np, name[dt], got.cpu().numpy(), params=prm, seed=5, offset=off,
+                      bitmask=bm_np, vocab_size=vocab, indices=idx_np, cols=V)
