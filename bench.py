@@ -11,15 +11,25 @@ One step = one in-place apply over a batch of the first workload plus one fused
 mask + sample over a batch of the second.  Inputs are resident in HBM and rotate
 through rings of copies larger than four L2 caches, so no step reads a batch
 from L2.  Steps are captured in CUDA graphs (launch gaps are those of a graph
-replay) and timed with CUDA events on the launching stream; CUDA events between
-the apply and sample graph replays split the time per kernel.
+replay; at most K/4 steps per graph, so a run times at least four replays) and
+timed with CUDA events on the launching stream; CUDA events between the apply
+and sample graph replays split the time per kernel.
+
+The default run then times every configuration of the benchmark list the same
+way, one after another (``configs`` in the output line): the tiny apply +
+greedy case, the apply workload, the fused workload with its apply alone, the
+Zipf top-p sweep (0.5, 0.9, 0.99 and greedy) and the speculative-verify batch
+with its apply alone.  Each figure carries its dense algorithmic bytes and the
+sector-minimal bytes counted from the actual mask.
 
     python bench.py [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload default|apply_only|fused_sample|zipf_top_p|
-                                speculative_verify|tiny_greedy]
+                                speculative_verify|tiny_greedy] [--top-p P]
 
-Prints one JSON line.  ``--impl reference`` times the CPU oracle (single
-thread) on a bounded sample of the same workload instead.
+Prints one JSON line.  ``cpu_baseline`` times the CPU oracle on bounded samples
+of the same workloads, on one thread and row-parallel on every host core.
+``--impl reference`` times the oracle, row-parallel on every host core, as the
+reference arm.
 """
 from __future__ import annotations
 
@@ -67,6 +77,56 @@ def sample_bytes(w: syn.Workload, masked: bool = True) -> int:
     if masked and w.bitmask is not None:
         b += apply_rows(w) * w.bitmask.shape[1] * 4
     return b
+
+
+def _applied_rows(w: syn.Workload) -> np.ndarray:
+    if w.indices is None:
+        return np.arange(w.B)
+    lim = min(w.B, w.bitmask.shape[0])
+    return np.unique(w.indices[(w.indices >= 0) & (w.indices < lim)])
+
+
+def _sector_flags(w: syn.Workload, b: int):
+    """(any kept, any masked) per 32-byte sector of row b's first vocab_size
+    tokens, from the row's mask bits (sectors aligned in memory)."""
+    eb = EB[w.dtype]
+    words = w.bitmask[b].view(np.uint32)
+    bits = np.unpackbits(words.view(np.uint8), bitorder="little")[:w.vocab_size].astype(bool)
+    phase = (b * w.stride * eb) % 32 // eb       # tokens before the row in its first sector
+    per = 32 // eb
+    n = phase + w.vocab_size
+    pad_kept = np.zeros(-(-n // per) * per, dtype=bool)
+    pad_mask = np.zeros_like(pad_kept)
+    pad_kept[phase:n] = bits
+    pad_mask[phase:n] = ~bits
+    return pad_kept.reshape(-1, per).any(1), pad_mask.reshape(-1, per).any(1)
+
+
+def sector_minimal_bytes(w: syn.Workload, kind: str) -> int:
+    """The bytes a mask-aware kernel must move, counted from the actual mask in
+    32-byte DRAM sectors.  In-place apply: every mask word of the applied rows,
+    a sector write wherever a token is masked, and a sector read to merge where
+    a sector mixes kept and masked tokens (all-kept sectors are not touched).
+    Fused mask + sample: the mask words of masked rows, the sectors of masked
+    rows that hold a kept token, every sector of unmasked rows, and the ids."""
+    eb = EB[w.dtype]
+    sec_row = -(-w.vocab_size * eb // 32)
+    if kind == "apply":
+        rows = _applied_rows(w)
+        total = rows.size * w.bitmask.shape[1] * 4
+        for b in rows:
+            kept, masked = _sector_flags(w, int(b))
+            total += 32 * int(masked.sum()) + 32 * int((kept & masked).sum())
+        return total
+    total = 8 * w.B
+    masked_rows = set() if w.bitmask is None else set(int(b) for b in _applied_rows(w))
+    for b in range(w.B):
+        if b in masked_rows:
+            kept, _ = _sector_flags(w, b)
+            total += w.bitmask.shape[1] * 4 + 32 * int(kept.sum())
+        else:
+            total += 32 * sec_row
+    return total
 
 
 def describe(w: syn.Workload) -> str:
@@ -257,6 +317,8 @@ class Op:
             self.ws = torch.zeros(max(1, ops.sample_workspace_bytes(tdt, w.B, w.cols)),
                                   dtype=torch.uint8, device=dev)
         self.bytes = touched
+        self.sector_minimal = sector_minimal_bytes(w, kind) if (
+            w.bitmask is not None or kind == "sample") else None
         self.units = w.B
         # kernels one call launches: the apply kernel; or the sampler's stream and
         # finish kernels per launch of at most 16384 rows
@@ -379,13 +441,145 @@ def e2e_sample(w: syn.Workload, steps: int, torch, ops) -> dict:
             "d2h_bytes_per_step": int(8 * w.B), "ms_per_step": round(sec * 1e3, 4)}
 
 
-def roofline(bytes_per_launch: int, sec_per_launch: float, peak: dict, traffic) -> dict:
+def roofline(bytes_per_launch: int, sec_per_launch: float, peak: dict, traffic,
+             sector_minimal: int | None = None) -> dict:
     achieved = bytes_per_launch / sec_per_launch / 1e9
-    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak["hbm_gbs"],
-            "unit": "GB/s", "frac": round(achieved / peak["hbm_gbs"], 4),
-            "peak_source": peak["source"], "traffic": traffic,
-            "algorithmic_bytes_per_launch": int(bytes_per_launch),
-            "us_per_launch": round(sec_per_launch * 1e6, 3)}
+    r = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak["hbm_gbs"],
+         "unit": "GB/s", "frac": round(achieved / peak["hbm_gbs"], 4),
+         "peak_source": peak["source"], "traffic": traffic,
+         "algorithmic_bytes_per_launch": int(bytes_per_launch),
+         "us_per_launch": round(sec_per_launch * 1e6, 3)}
+    if sector_minimal is not None:
+        r["sector_minimal_bytes_per_launch"] = int(sector_minimal)
+        r["frac_sector_minimal"] = round(sector_minimal / sec_per_launch / 1e9 / peak["hbm_gbs"], 4)
+    return r
+
+
+class Timer:
+    """Times a plan of ops: K steps in CUDA graphs of G steps, each replay
+    bracketed by CUDA events on the launching stream, an untimed write of twice
+    the L2 before every replay, W warm-up steps first."""
+
+    def __init__(self, torch, l2: int):
+        self.torch, self.l2 = torch, l2
+        self.flush = torch.empty(2 * l2, dtype=torch.uint8, device="cuda")
+        self.clean = torch.zeros(2 * l2 // 4, dtype=torch.int32, device="cuda")
+
+    def empty_l2(self, r: int):
+        """Untimed: a write of twice the L2 evicts every input, then a read of
+        another twice the L2 writes those dirty lines back, so that the timed
+        kernels neither find their inputs in L2 nor pay for the flush's own
+        write-back."""
+        self.flush.fill_(r & 0xFF)
+        self.sink = self.clean.sum()
+
+    def run(self, plan, K: int, W: int, G: int, sampler=None):
+        torch = self.torch
+        graphs = [op.capture(G, 0) for op in plan]
+        rem = K % G
+        rem_graphs = [op.capture(rem, (K // G) * G) for op in plan] if rem else None
+        for _ in range(max(1, -(-W // G))):
+            for g in graphs:
+                g.replay()
+        torch.cuda.synchronize()
+        if sampler is not None:
+            sampler.start()
+        barrier()
+        torch.cuda.synchronize()
+        reps = K // G
+        nrep = reps + (1 if rem else 0)
+        ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+        marks = [[(ev(), ev()) for _ in plan] for _ in range(nrep)]
+        for r in range(nrep):
+            for i, g in enumerate(graphs if r < reps else rem_graphs):
+                self.empty_l2(r)
+                marks[r][i][0].record()
+                g.replay()
+                marks[r][i][1].record()
+        torch.cuda.synchronize()
+        barrier()
+        clocks = sampler.stop() if sampler is not None else None
+        per_op = [0.0] * len(plan)
+        for row in marks:
+            for i, (b, e) in enumerate(row):
+                per_op[i] += b.elapsed_time(e) / 1e3
+        dev = torch.device("cuda")
+        total = reduce_max(sum(per_op), dev)
+        per_op = [reduce_max(t, dev) for t in per_op]
+        del graphs, rem_graphs
+        return per_op, total, clocks, nrep
+
+
+def graph_len(args) -> int:
+    """Steps per graph: at most --graph-steps, and at most K/4 so that even a short
+    run times at least four replays."""
+    return max(1, min(args.graph_steps, args.steps // 4 if args.steps >= 4 else 1))
+
+
+def op_line(op, sec: float, ws: int, peak: dict) -> dict:
+    """One op's figures: time per launch, throughput and its roofline (dense and
+    sector-minimal bytes)."""
+    wl = op.w.name
+    knames = (["apply_kernel"] if op.kind == "apply" else
+              ["sample_stream_kernel", "sample_finish_kernel"])
+    rf = roofline(op.bytes, sec, peak, ncu_traffic(knames, wl), op.sector_minimal)
+    line = {"workload": describe(op.w), "us_per_launch": round(sec * 1e6, 3), "roofline": rf}
+    if op.kind == "apply":
+        line.update(value=round(whole_job_rate(op.bytes, ws, sec) / 1e9, 2), unit="GB/s")
+    else:
+        line.update(value=round(whole_job_rate(op.units, ws, sec), 1), unit="rows/s",
+                    GBps_algorithmic=rf["achieved"])
+    return line
+
+
+# The per-configuration block of the default run: every configuration of the
+# benchmark list, each sampler sub-run and the apply legs, timed one after another.
+CONFIGS = [
+    ("C1 tiny_greedy (launch-bound; latency reported)", "tiny_greedy", None, ("apply", "sample")),
+    ("C2 apply_only", "apply_only", None, ("apply",)),
+    ("C3 fused_sample", "fused_sample", None, ("sample", "apply")),
+    ("C4 zipf_top_p top_p 0.5", "zipf_top_p", 0.5, ("sample",)),
+    ("C4 zipf_top_p top_p 0.9", "zipf_top_p", 0.9, ("sample",)),
+    ("C4 zipf_top_p top_p 0.99", "zipf_top_p", 0.99, ("sample",)),
+    ("C4 zipf_top_p greedy", "zipf_top_p", "greedy", ("sample",)),
+    ("C5 speculative_verify", "speculative_verify", None, ("sample", "apply")),
+]
+
+
+def config_workload(name: str, top_p, base: syn.Workload | None = None):
+    w = make_workload(name) if base is None else base
+    if name == "zipf_top_p":
+        w.temperature, w.top_p = 0.7, 0.9
+        if top_p == "greedy":
+            w.temperature = 0.0
+        elif top_p is not None:
+            w.top_p = float(top_p)
+    return w
+
+
+def run_configs(args, timer, torch, ops, ring_min: int, peak: dict, ws: int,
+                dev_id) -> dict:
+    K, W, G = args.steps, args.warmup, graph_len(args)
+    out = {}
+    base = None
+    for label, name, tp, kinds in CONFIGS:
+        if base is None or base.name != name:
+            base = None
+            torch.cuda.empty_cache()
+        base = config_workload(name, tp, base)
+        w = base
+        plan = [Op(k, w, ring_min, torch, ops, G if k == "apply" else 2) for k in kinds]
+        per_op, _, clocks, nrep = timer.run(plan, K, W, G, ClockSampler(dev_id))
+        entry = {}
+        for op, t in zip(plan, per_op):
+            entry["fused_mask_sample" if op.kind == "sample" and w.bitmask is not None
+                  else ("sample" if op.kind == "sample" else "apply")] = op_line(op, t / K, ws, peak)
+        entry["gpu_launches"] = K * sum(op.kernels for op in plan)
+        entry["replays"] = nrep
+        entry["clocks"] = clocks
+        out[label] = entry
+        del plan
+    return out
 
 
 def run_gpu(args) -> dict | None:
@@ -405,9 +599,9 @@ def run_gpu(args) -> dict | None:
     l2 = int(getattr(dev_props, "L2_cache_size", 128 << 20))
     ring_min = 4 * l2
     K, W = args.steps, args.warmup
-    G = max(1, min(args.graph_steps, K))
+    G = graph_len(args)
 
-    plan = []  # (op, units label)
+    plan = []
     if args.workload == "default":
         wa, wf = make_workload("apply_only"), make_workload("fused_sample")
         plan = [Op("apply", wa, ring_min, torch, ops, G), Op("sample", wf, ring_min, torch, ops)]
@@ -418,25 +612,10 @@ def run_gpu(args) -> dict | None:
         w = make_workload("tiny_greedy")
         plan = [Op("apply", w, ring_min, torch, ops), Op("sample", w, ring_min, torch, ops)]
     else:
-        w = make_workload(args.workload)
-        if args.workload == "zipf_top_p":
-            if args.top_p == "greedy":
-                w.temperature = 0.0
-            else:
-                w.top_p = float(args.top_p)
+        w = config_workload(args.workload, args.top_p if args.workload == "zipf_top_p" else None)
         plan = [Op("sample", w, ring_min, torch, ops)]
-
-    graphs = [op.capture(G, 0) for op in plan]
-    # an untimed write of twice the L2 before every graph replay: no replay finds
-    # its inputs (or an earlier replay's) in L2
-    flush = torch.empty(2 * l2, dtype=torch.uint8, device="cuda")
-    rem = K % G
-    rem_graphs = [op.capture(rem, (K // G) * G) for op in plan] if rem else None
-
-    for _ in range(max(1, -(-W // G))):
-        for g in graphs:
-            g.replay()
-    torch.cuda.synchronize()
+        if args.apply_leg and w.bitmask is not None:
+            plan.append(Op("apply", w, ring_min, torch, ops, G))
 
     dev_id = None
     try:
@@ -445,31 +624,9 @@ def run_gpu(args) -> dict | None:
             dev_id = "GPU-" + dev_id
     except Exception:  # noqa: BLE001
         dev_id = os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0] or None
-    sampler = ClockSampler(dev_id)
-    sampler.start()
-    barrier()
-    torch.cuda.synchronize()
-    reps = K // G
-    nrep = reps + (1 if rem else 0)
-    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    marks = [[(ev(), ev()) for _ in plan] for _ in range(nrep)]
-    for r in range(nrep):
-        for i, g in enumerate(graphs if r < reps else rem_graphs):
-            flush.fill_(r & 0xFF)
-            marks[r][i][0].record()
-            g.replay()
-            marks[r][i][1].record()
-    torch.cuda.synchronize()
-    barrier()
-    clocks = sampler.stop()
-
-    per_op = [0.0] * len(plan)
-    for row in marks:
-        for i, (b, e) in enumerate(row):
-            per_op[i] += b.elapsed_time(e) / 1e3
-    total_s = reduce_max(sum(per_op), torch.device("cuda"))
-    per_op = [reduce_max(t, torch.device("cuda")) for t in per_op]
-    if rank != 0:
+    timer = Timer(torch, l2)
+    per_op, total_s, clocks, nrep = timer.run(plan, K, W, G, ClockSampler(dev_id))
+    if rank != 0 and args.workload != "default":
         return None
 
     peak = measured_peaks()
@@ -478,11 +635,13 @@ def run_gpu(args) -> dict | None:
            "scaling": "weak", "vs_baseline": None, "dtype": plan[0].w.dtype,
            "data": "synthetic (seeded generators shaped like the pages' workloads)",
            "gpu_launches": K * sum(op.kernels for op in plan) * ws}
-    cfg = {"workload": " + ".join(describe(op.w) for op in plan),
-           "l2": f"an untimed write of 2x the {l2 >> 20} MB L2 before every graph replay, and "
-                 "inputs in device rings (>= 4x the L2; an apply's copies do not repeat within "
-                 "a graph), so no step reads its batch from L2",
-           "timing": f"CUDA graphs of {G} steps replayed; CUDA events on the launch stream",
+    cfg = {"workload": " + ".join(describe(op.w) + f" [{op.kind}]" for op in plan),
+           "l2": f"an untimed write of 2x the {l2 >> 20} MB L2, then a read of another 2x, "
+                 "before every graph replay, and inputs in device rings (>= 4x the L2; an "
+                 "apply's copies do not repeat within a graph), so no step reads its batch "
+                 "from L2",
+           "timing": f"CUDA graphs of {G} steps, {nrep} replays; CUDA events on the launch "
+                     "stream",
            "parallelism": f"replicas x{ws} (rows shard with no collective)"}
     for op in plan:
         cfg[f"ring_{op.kind}"] = op.R
@@ -491,28 +650,13 @@ def run_gpu(args) -> dict | None:
     res["config"] = cfg
     lines = {}
     for op, t in zip(plan, per_op):
-        sec = t / K
-        wl = op.w.name
-        knames = (["apply_kernel"] if op.kind == "apply" else
-                  ["sample_stream_kernel", "sample_finish_kernel"])
-        rf = roofline(op.bytes, sec, peak, ncu_traffic(knames, wl))
-        if op.kind == "apply":
-            lines["apply"] = {"value": round(whole_job_rate(op.bytes, ws, sec) / 1e9, 2),
-                              "unit": "GB/s",
-                              "workload": describe(op.w), "roofline": rf}
-        else:
-            lines["sample"] = {"value": round(whole_job_rate(op.units, ws, sec), 1),
-                               "unit": "rows/s",
-                               "workload": describe(op.w), "roofline": rf,
-                               "GBps_algorithmic": rf["achieved"]}
-    if "apply" in lines:
-        res["value"] = lines["apply"]["value"]
-        res["unit"] = "GB/s"
+        lines.setdefault(op.kind, op_line(op, t / K, ws, peak))
+    if "apply" in lines and args.workload in ("default", "apply_only", "tiny_greedy"):
+        res["value"], res["unit"] = lines["apply"]["value"], "GB/s"
     else:
-        res["value"] = lines["sample"]["value"]
-        res["unit"] = "rows/s"
+        res["value"], res["unit"] = lines["sample"]["value"], "rows/s"
     dominant = max(zip(plan, per_op), key=lambda x: x[1])[0]
-    res["roofline"] = lines["apply" if dominant.kind == "apply" else "sample"]["roofline"]
+    res["roofline"] = dict(lines[dominant.kind]["roofline"])
     res["roofline"]["kernel"] = (
         "apply_kernel" if dominant.kind == "apply" else
         "lp_mask_and_sample call: sample_stream_kernel + sample_finish_kernel, timed together")
@@ -525,31 +669,96 @@ def run_gpu(args) -> dict | None:
     if not args.no_e2e:
         e2e = {}
         for op in plan:
-            if op.kind == "apply":
+            if op.kind == "apply" and "apply" not in e2e:
                 e2e["apply"] = e2e_apply(op.w, args.e2e_steps, torch, ops)
-            else:
+            elif op.kind == "sample" and "sample" not in e2e:
                 e2e["sample"] = e2e_sample(op.w, args.e2e_steps, torch, ops)
-        head = e2e.get("apply") or e2e.get("sample")
+        head = e2e.get("apply") if res["unit"] == "GB/s" else e2e.get("sample")
         res["e2e"] = {"value": head["value"], "unit": head["unit"],
                       "h2d_bytes_per_step": sum(v["h2d_bytes_per_step"] for v in e2e.values()),
                       "d2h_bytes_per_step": sum(v["d2h_bytes_per_step"] for v in e2e.values()),
                       "parts": e2e}
+    del plan
+    torch.cuda.empty_cache()
+    if args.workload == "default" and not args.no_configs:
+        res["configs"] = run_configs(args, timer, torch, ops, ring_min, peak, ws, dev_id)
+    if rank != 0:
+        return None
     if not args.no_cpu_baseline and ws == 1:
-        res["cpu_baseline"] = cpu_baseline([op.w for op in plan], [op.kind for op in plan],
-                                           args.cpu_seconds)
+        res["cpu_baseline"] = cpu_baseline(args)
     return res
 
 
 # -------------------------------------------------------------- CPU oracle
 
-def _oracle_apply_rows(w: syn.Workload, nrows: int):
-    """Oracle apply restricted to the first nrows of the workload's row list."""
-    import oracle
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
 
-    idx = w.indices if w.indices is not None else np.arange(w.B, dtype=np.int32)
-    sub = idx[:nrows]
-    return lambda: oracle.apply(w.logits, w.bitmask, dtype={"f32": 0, "f16": 1, "bf16": 2}[w.dtype],
-                                vocab_size=w.vocab_size, indices=sub, cols=w.cols)
+
+def _time_for(fn, seconds: float):
+    fn()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= seconds:
+            return dt / n, n
+
+
+class OracleJob:
+    """One bounded sample of a workload run by the CPU oracle, as it stands, on
+    ``threads`` host threads: the rows are split into one contiguous share per
+    thread, and each thread runs the oracle's C code on its share (the binding
+    releases the interpreter lock during the call)."""
+
+    def __init__(self, kind: str, w: syn.Workload, threads: int, rows_per_thread: int = 0):
+        import oracle
+
+        self.kind, self.w, self.threads = kind, w, max(1, threads)
+        dt = {"f32": 0, "f16": 1, "bf16": 2}[w.dtype]
+        if kind == "apply":
+            rows = _applied_rows(w).astype(np.int32)
+            self.rows = rows
+            self.out = w.logits.copy()
+            shares = [c for c in np.array_split(rows, self.threads) if c.size]
+            self.calls = [
+                (lambda c=c: oracle.apply(w.logits, w.bitmask, dtype=dt, vocab_size=w.vocab_size,
+                                          indices=c, cols=w.cols, out=self.out))
+                for c in shares]
+            self.units = apply_bytes(w) * rows.size / max(apply_rows(w), 1)
+            self.desc = f"all {rows.size} applied rows"
+        else:
+            nr = min(w.B, max(1, rows_per_thread) * self.threads)
+            rows = np.sort(np.random.default_rng(0).choice(w.B, size=nr, replace=False))
+            self.rows = rows
+            shares = [c for c in np.array_split(rows, self.threads) if c.size]
+            self.calls = [_oracle_sample_rows(w, c) for c in shares]
+            self.units = float(nr)
+            self.desc = f"{nr} seeded rows"
+        self.pool = None
+        if len(self.calls) > 1:
+            from concurrent.futures import ThreadPoolExecutor
+
+            self.pool = ThreadPoolExecutor(len(self.calls))
+
+    def __call__(self):
+        if self.pool is None:
+            self.calls[0]()
+        else:
+            list(self.pool.map(lambda f: f(), self.calls))
+
+    def close(self):
+        if self.pool is not None:
+            self.pool.shutdown()
+
+    def rate(self, sec: float):
+        if self.kind == "apply":
+            return round(self.units / sec / 1e9, 4), "GB/s"
+        return round(self.units / sec, 3), "rows/s"
 
 
 def _oracle_sample_rows(w: syn.Workload, rows: np.ndarray, offset: int = 0):
@@ -564,101 +773,92 @@ def _oracle_sample_rows(w: syn.Workload, rows: np.ndarray, offset: int = 0):
         top_p=pr["top_p"], min_p=pr["min_p"], seed=w.seed, offset=offset, row_ids=rows)
 
 
-def _time_for(fn, seconds: float):
-    fn()
-    n, t0 = 0, time.perf_counter()
-    while True:
-        fn()
-        n += 1
-        dt = time.perf_counter() - t0
-        if dt >= seconds:
-            return dt / n, n
+def bench_workloads(workload: str, top_p="0.9"):
+    """(kind, workload) pairs of a bench run: the headline apply and fused
+    workloads by default, else the selected one."""
+    if workload == "default":
+        return [("apply", make_workload("apply_only")), ("sample", make_workload("fused_sample"))]
+    if workload == "apply_only":
+        return [("apply", make_workload("apply_only"))]
+    if workload == "tiny_greedy":
+        w = make_workload("tiny_greedy")
+        return [("apply", w), ("sample", w)]
+    return [("sample", config_workload(workload, top_p if workload == "zipf_top_p" else None))]
 
 
-def cpu_baseline(workloads, kinds, seconds: float) -> dict:
-    """The oracle, as it stands (single thread), on bounded samples."""
+def cpu_baseline(args) -> dict:
+    """The oracle, as it stands, on bounded samples of the bench's workloads: on
+    one thread, and row-parallel on every core of this process's affinity set."""
+    cores = host_cores()
     parts = {}
-    per = seconds / max(len(workloads), 1)
-    for w, kind in zip(workloads, kinds):
-        if kind == "apply":
-            rows = apply_rows(w)
-            per_call, n = _time_for(_oracle_apply_rows(w, rows), per)
-            gbs = apply_bytes(w) / per_call / 1e9
-            parts["apply"] = {"value": round(gbs, 4), "unit": "GB/s",
-                              "sample": f"{describe(w)}: all {rows} applied rows, {n} repeats"}
-        else:
-            nr = min(w.B, 16)
-            rows = np.sort(np.random.default_rng(0).choice(w.B, size=nr, replace=False))
-            per_call, n = _time_for(_oracle_sample_rows(w, rows), per)
-            parts["sample"] = {"value": round(nr / per_call, 3), "unit": "rows/s",
-                               "sample": f"{describe(w)}: {nr} seeded rows, {n} repeats"}
-    head = parts.get("apply") or parts.get("sample")
-    return {"value": head["value"], "unit": head["unit"], "cores": 1, "kind": "oracle",
-            "sample": head["sample"], "parts": parts}
+    jobs = bench_workloads(args.workload, args.top_p)
+    per = args.cpu_seconds / max(2 * len(jobs), 1)
+    for kind, w in jobs:
+        for threads in (1, cores):
+            job = OracleJob(kind, w, threads, rows_per_thread=16 if threads == 1 else 4)
+            sec, n = _time_for(job, per)
+            job.close()
+            v, u = job.rate(sec)
+            parts[f"{kind}_{threads}_threads"] = {
+                "value": v, "unit": u, "cores": threads,
+                "sample": f"{describe(w)}: {job.desc}, {n} repeats"}
+    lead = parts[f"{jobs[0][0]}_{cores}_threads"]
+    return {"value": lead["value"], "unit": lead["unit"], "cores": cores, "kind": "oracle",
+            "sample": lead["sample"] + f"; row-parallel over {cores} host threads, the "
+                                       "single-thread figures beside it in parts",
+            "parts": parts}
 
 
 def run_reference(args) -> dict | None:
-    """The oracle timed as the reference arm: each step one bounded sample of the
-    workload (apply rows and sampled rows sized so the run stays in minutes)."""
+    """The oracle timed as the reference arm, row-parallel on every host core:
+    each step one bounded sample of the workload (the applied rows, or seeded
+    sampled rows, sized so the run stays in minutes)."""
     ws, rank, _ = dist_env()
     if rank != 0:
         return None
     import oracle
 
     oracle.build()
-    if args.workload in ("default",):
-        ws_list = [("apply", make_workload("apply_only")), ("sample", make_workload("fused_sample"))]
-    elif args.workload == "apply_only":
-        ws_list = [("apply", make_workload("apply_only"))]
-    elif args.workload == "tiny_greedy":
-        w = make_workload("tiny_greedy")
-        ws_list = [("apply", w), ("sample", w)]
-    else:
-        ws_list = [("sample", make_workload(args.workload))]
+    cores = host_cores()
+    jobs_in = bench_workloads(args.workload, args.top_p)
     K, W = args.steps, args.warmup
-    budget = args.reference_seconds / max(K + W, 1)   # seconds per step
-    calls = []
-    for kind, w in ws_list:
+    budget = args.reference_seconds / max(K + W, 1) / len(jobs_in)   # seconds per call
+    jobs = []
+    for kind, w in jobs_in:
         if kind == "apply":
-            total_rows = apply_rows(w)
-            t1, _ = _time_for(_oracle_apply_rows(w, 1), 0.2)
-            nr = int(max(1, min(total_rows, budget / len(ws_list) / max(t1, 1e-9))))
-            fn = _oracle_apply_rows(w, nr)
-            frac = nr / total_rows
-            calls.append((kind, w, fn, apply_bytes(w) * frac, nr))
+            jobs.append(OracleJob(kind, w, cores))
         else:
-            t1, _ = _time_for(_oracle_sample_rows(w, np.array([0])), 0.2)
-            nr = int(max(1, min(w.B, budget / len(ws_list) / max(t1, 1e-9))))
-            rows = np.sort(np.random.default_rng(0).choice(w.B, size=nr, replace=False))
-            calls.append((kind, w, _oracle_sample_rows(w, rows), nr, nr))
-    times = [0.0] * len(calls)
+            probe = OracleJob(kind, w, 1, rows_per_thread=1)
+            t1, _ = _time_for(probe, 0.2)
+            per_thread = int(max(1, min(-(-w.B // cores), budget / max(t1, 1e-9))))
+            jobs.append(OracleJob(kind, w, cores, rows_per_thread=per_thread))
+    times = [0.0] * len(jobs)
     for _ in range(W):
-        for _, _, fn, _, _ in calls:
-            fn()
+        for job in jobs:
+            job()
     for _ in range(K):
-        for i, (_, _, fn, _, _) in enumerate(calls):
+        for i, job in enumerate(jobs):
             t0 = time.perf_counter()
-            fn()
+            job()
             times[i] += time.perf_counter() - t0
+    for job in jobs:
+        job.close()
     res = {"impl": "reference", "metric": METRIC, "n_gpus": 1, "steps": K, "warmup": W,
            "ms_per_step": round(sum(times) / max(K, 1) * 1e3, 4), "higher_is_better": True,
-           "scaling": "weak", "vs_baseline": None, "dtype": ws_list[0][1].dtype,
+           "scaling": "weak", "vs_baseline": None, "dtype": jobs_in[0][1].dtype,
            "data": "synthetic (seeded generators shaped like the pages' workloads)",
            "gpu_launches": 0}
     parts = {}
-    for (kind, w, _, units, nr), t in zip(calls, times):
-        sec = t / max(K, 1)
-        if kind == "apply":
-            parts["apply"] = {"value": round(units / sec / 1e9, 4), "unit": "GB/s",
-                              "sample": f"{describe(w)}: {nr} of {apply_rows(w)} applied rows per step"}
-        else:
-            parts["sample"] = {"value": round(units / sec, 3), "unit": "rows/s",
-                               "sample": f"{describe(w)}: {nr} seeded rows per step"}
+    for job, t in zip(jobs, times):
+        v, u = job.rate(t / max(K, 1))
+        parts[job.kind] = {"value": v, "unit": u,
+                           "sample": f"{describe(job.w)}: {job.desc} per step, row-parallel "
+                                     f"over {cores} host threads"}
     head = parts.get("apply") or parts.get("sample")
     res["value"], res["unit"] = head["value"], head["unit"]
-    res["config"] = {"workload": " + ".join(describe(w) for _, w in ws_list),
-                     "parallelism": "single CPU thread"}
-    res["cpu_baseline"] = {"value": head["value"], "unit": head["unit"], "cores": 1,
+    res["config"] = {"workload": " + ".join(describe(w) for _, w in jobs_in),
+                     "parallelism": f"CPU oracle, row-parallel over {cores} host threads"}
+    res["cpu_baseline"] = {"value": head["value"], "unit": head["unit"], "cores": cores,
                            "kind": "oracle", "sample": head["sample"], "parts": parts}
     res["e2e"] = {"value": head["value"], "unit": head["unit"], "h2d_bytes_per_step": 0,
                   "d2h_bytes_per_step": 0}
@@ -670,8 +870,8 @@ def run_reference(args) -> dict | None:
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="default",
                     choices=["default", *syn.WORKLOADS.keys()])
@@ -685,6 +885,10 @@ def main(argv=None):
                     help="apply_only: select the rows by per-row flags and report which keep a "
                          "token (lp_apply_token_bitmask_rows) instead of indices")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="default run: skip the per-configuration block")
+    ap.add_argument("--apply-leg", action="store_true",
+                    help="a sampler workload with a mask: also time the in-place apply alone")
     args = ap.parse_args(argv)
     res = run_reference(args) if args.impl == "reference" else run_gpu(args)
     if res is not None:

@@ -71,5 +71,33 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB
 
 
+def build_variant(name: str, defines: dict, sources=("sample.cu",), force: bool = False) -> str:
+    """A test build: the given csrc sources compiled with extra preprocessor
+    definitions and linked as ``_build/<name>/liblp.so``.  Test builds exercise
+    paths that the product build cannot reach on demand (a bounded wait made to
+    run out); the product library ``liblp.so`` is never one of them."""
+    nvcc = _nvcc()
+    out_dir = os.path.join(BUILD, name)
+    os.makedirs(out_dir, exist_ok=True)
+    srcs = [os.path.join(CSRC, x) for x in sources]
+    headers = sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + [os.path.join(INCLUDE, "lp.h")]
+    lib = os.path.join(out_dir, "liblp.so")
+    defs = [f"-D{k}={v}" for k, v in sorted(defines.items())]
+    stamp = os.path.join(out_dir, "defines.txt")
+    same = os.path.exists(stamp) and open(stamp).read() == " ".join(defs)
+    if force or not same or _stale(lib, srcs + headers):
+        objs = []
+        for src in srcs:
+            obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
+            subprocess.check_call([nvcc, *ARCH, *FLAGS, *defs, "-c", src, "-o", obj])
+            objs.append(obj)
+        tmp = lib + f".tmp{os.getpid()}"
+        subprocess.check_call([nvcc, *ARCH, "-shared", "-o", tmp, *objs])
+        os.replace(tmp, lib)
+        with open(stamp, "w") as f:
+            f.write(" ".join(defs))
+    return lib
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose=True))

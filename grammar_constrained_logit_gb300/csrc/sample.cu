@@ -490,6 +490,17 @@ __device__ __forceinline__ bool row_masked(const SampleArgs& a, int row) {
 
 // ================================================================ stream kernel
 
+// Bounded poll of a shared-memory hand-over counter: true once *p == target,
+// false after `limit` polls of 64 ns sleeps.
+constexpr uint32_t kFreshPolls = kMaxWaitTries * 64u;
+__device__ __forceinline__ bool poll_fresh(const int* p, int target, uint32_t limit) {
+  for (uint32_t t = 0; *(const volatile int*)p != target; ++t) {
+    if (t >= limit) return false;
+    __nanosleep(64);
+  }
+  return true;
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t* m) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(m)) : "memory");
 }
@@ -646,14 +657,21 @@ __global__ void __launch_bounds__(kThreads, 3) sample_stream_kernel(const Sample
     const float T = rp.T, c2 = rp.c2, delta = rp.delta;
 
     // this parity's state is ready once the last warp of tile it - 2 has reset
-    // it (bounded wait; the warps of a CTA are at most a few pieces apart)
+    // it (bounded wait; the warps of a CTA are at most a few pieces apart).  A
+    // wait that gives up marks the CTA's tiles from here on as failed (their
+    // rows report -2), then waits once more, also bounded, so that the state is
+    // still left alone until it is handed over.
     if (lane == 0) {
-      for (uint32_t t = 0; *(volatile int*)&s_fresh[par] != it; ++t) {
-        if (t > kMaxWaitTries * 64u) {
-          s_err = 1;
-          break;
-        }
-        __nanosleep(64);
+      bool ok = poll_fresh(&s_fresh[par], it, kFreshPolls);
+#ifdef LP_TEST_FRESH_TIMEOUT
+      // test builds only: one wait of CTA 0 polls for a hand-over that never
+      // comes, LP_TEST_FRESH_TIMEOUT times, and so runs out
+      if (ok && blockIdx.x == 0 && it == 1)
+        ok = poll_fresh(&s_fresh[par], it + (1 << 30), LP_TEST_FRESH_TIMEOUT);
+#endif
+      if (!ok) {
+        s_err = 1;
+        (void)poll_fresh(&s_fresh[par], it, kFreshPolls);
       }
       __threadfence_block();
     }
