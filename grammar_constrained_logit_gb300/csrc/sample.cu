@@ -72,8 +72,8 @@ constexpr int64_t kTileTarget = 1024;    // tiles per launch that shorter tiles 
 constexpr int kCompactBytes = 24576;     // shared memory of the compaction buffers
 constexpr int kSlotCap = 256;            // entries a tile keeps in its own workspace slot
 constexpr int kStage = 4096;             // buffered entries a finishing CTA stages
-constexpr int kWinBins = 256;            // bins of the fallback's window search (one per thread)
-static_assert(kWinBins == kThreads, "one window bin per thread");
+constexpr int kWinBins = 2048;           // bins of the fallback's window search
+static_assert(kWinBins % kThreads == 0, "whole bins per thread");
 constexpr int kMetaCap = 1024;           // tiles per row whose buffer starts it stages
 constexpr int kFinishSmem = kStage * 8 + (kMetaCap + 1) * 4;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -1324,24 +1324,36 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
     }
   };
   // Re-reads the whole row from global memory: f(raw, cb, i0) per vector,
-  // warp-uniform.
+  // warp-uniform.  Each thread loads the bitmask words and logits of kReread
+  // vectors (independent loads) before it works on any of them, so the loads of
+  // a pass overlap instead of running one round trip after another.
   Sp rw;
   bool rw_ready = false;
+  constexpr int kReread = 2;
   auto reread = [&](auto&& f) {
     if (!rw_ready) {
       rw.init(a, row, 0, a.V, row_masked(a, row));
       rw_ready = true;
     }
-    for (int base = 0; base < rw.nvec; base += kThreads) {
-      const int q = base + tid;
-      int i0 = 0;
-      uint32_t cb = 0;
-      uint4 raw = make_uint4(0, 0, 0, 0);
-      if (q < rw.nvec) {
-        cb = rw.bits(q, i0, nullptr, 0, 0);
-        if (cb) raw = rw.gvec(q);
+    for (int base = 0; base < rw.nvec; base += kThreads * kReread) {
+      uint4 raw[kReread];
+      uint32_t cb[kReread];
+#pragma unroll
+      for (int u = 0; u < kReread; ++u) {
+        const int q = base + u * kThreads + tid;
+        int i0 = 0;
+        cb[u] = 0u;
+        raw[u] = make_uint4(0, 0, 0, 0);
+        if (q < rw.nvec) {
+          cb[u] = rw.bits(q, i0, nullptr, 0, 0);
+          raw[u] = rw.gvec(q);
+        }
       }
-      f(raw, cb, i0);
+#pragma unroll
+      for (int u = 0; u < kReread; ++u) {
+        const int q = base + u * kThreads + tid;
+        f(raw[u], cb[u], (16 * q - rw.mis) / Sp::EB);
+      }
     }
   };
 
@@ -1358,8 +1370,100 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
   // (top-p), counting candidates of the tiles' buffers or of a re-read of the
   // row.  False when none exists.
   // Over [lo, hi], with above_c0 / above_m0 already counted above hi.
+  // Narrows a descent over the buffered entries.  One pass sums the count, the
+  // exact fixed-point mass and the smallest and largest key of the entries in
+  // [lo, hi] per bin of kThreads bins of equal width in value (bin 0 at the
+  // top); the range shrinks to the entries of the first bin from the top at
+  // which a target is reached, and the entries above them are counted.  Bins of
+  // equal width spread the entries over many addresses, where the first digits
+  // of the key (sign and exponent bits) would put most of them in a few bins and
+  // serialize the atomics.  Bins are monotone in the value, so the entries above
+  // the bin's largest key are exactly those of the bins before it.  False when
+  // no target is reached in [lo, hi].
+  __shared__ unsigned s_kmin[kThreads], s_kmax[kThreads];
+  __shared__ float s_nlo, s_nhi;
+  auto narrow = [&](float& lo, float& hi, unsigned& above_c, unsigned long long& above_m) -> bool {
+    const float top = fminf(hi, lmax);
+    if (!(top > lo)) return true;  // a single value: nothing to narrow
+    const float bpl = float(kThreads) / (top - lo);
+    const int hp = npass & 1;
+    ++npass;
+    hist.cnt[hp][tid] = 0u;
+    if (limbs) {
+      hist.limb[hp][tid][0] = 0u;
+      hist.limb[hp][tid][1] = 0u;
+      hist.limb[hp][tid][2] = 0u;
+    } else {
+      hist.mass[hp][tid] = 0ull;
+    }
+    s_kmin[tid] = 0xffffffffu;
+    s_kmax[tid] = 0u;
+    if (tid == 0) s_sel = INT_MAX;
+    __syncthreads();
+    const float lo0 = lo;
+    buffered([&](float x, int, bool ok) {
+      if (!(ok && x >= lo0 && x <= top)) return;
+      const int b = min(max(int((top - x) * bpl), 0), kThreads - 1);
+      if (has_p) {
+        const unsigned long long mm = mass40(x, lmax, c2);
+        if (limbs)
+          limb_add(hist.limb[hp][b], mm);
+        else
+          atomicAdd(&hist.mass[hp][b], mm);
+      }
+      atomicAdd(&hist.cnt[hp][b], 1u);
+      const uint32_t kx = fkey(x);
+      atomicMin(&s_kmin[b], kx);
+      atomicMax(&s_kmax[b], kx);
+    });
+    __syncthreads();
+    const unsigned c = hist.cnt[hp][tid];
+    const unsigned long long m = limbs ? limb_sum(hist.limb[hp][tid]) : hist.mass[hp][tid];
+    unsigned ic = c;
+    unsigned long long im = m;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned yc = __shfl_up_sync(kFullWarp, ic, o);
+      const unsigned long long ym = __shfl_up_sync(kFullWarp, im, o);
+      if (lane >= o) {
+        ic += yc;
+        im += ym;
+      }
+    }
+    if (lane == 31) {
+      scan_c[warp] = ic;
+      scan_m[warp] = im;
+    }
+    __syncthreads();
+    for (int w = 0; w < warp; ++w) {
+      ic += scan_c[w];
+      im += scan_m[w];
+    }
+    const unsigned cc = above_c + ic;
+    const unsigned long long cm = above_m + im;
+    if (c > 0u && ((sel_k > 0 && cc >= unsigned(sel_k)) || (has_p && cm >= sel_P)))
+      atomicMin(&s_sel, tid);
+    __syncthreads();
+    const int b = s_sel;
+    if (b == INT_MAX) return false;
+    if (tid == b) {
+      s_above_c = cc - c;
+      s_above_m = cm - m;
+      s_nlo = key_float(s_kmin[b]);
+      s_nhi = key_float(s_kmax[b]);
+    }
+    __syncthreads();
+    above_c = s_above_c;
+    above_m = s_above_m;
+    lo = s_nlo;
+    hi = s_nhi;
+    __syncthreads();  // every thread has its copy before the shared words are reused
+    return true;
+  };
+
   auto descend = [&](bool from_buffers, float lo, uint32_t& out_key, float hi = INFINITY,
                      unsigned above_c0 = 0u, unsigned long long above_m0 = 0ull) -> bool {
+    if (from_buffers && !narrow(lo, hi, above_c0, above_m0)) return false;
     const uint32_t klo = fkey(lo), khi = fkey(fminf(hi, lmax));
     const uint32_t diff = klo ^ khi;
     int top = diff ? 32 - __clz(diff) : kLow + 1;  // one past the highest differing bit
@@ -1386,7 +1490,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
       // element x (when part) into its bin: one 32-bit atomic for the count and,
       // for top-p rows, three for the mass limbs (or one 64-bit atomic)
       auto add = [&](float x, bool part) {
-        if (!(part && x >= lo)) return;
+        if (!(part && x >= lo && x <= hi)) return;
         const uint32_t kx = fkey(x);
         if (((kx ^ prefix) & himask) != 0u) return;
         const int d = int((kx >> shift) & dmask);
@@ -1462,24 +1566,26 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
 
 
   // ---------------------- a window around the threshold (top-p rows, re-read)
-  // For float32 logits (four radix passes over the row), two re-reads of the row
-  // stand in for a radix pass per key digit.  The first
+  // Two re-reads of the row stand in for a radix pass per key digit.  The first
   // sums the candidates' softmax mass and count in kWinBins equal bins of
-  // (lmax - x) / T down to fcut (per-warp bins, fp32 sums); the bin where the
-  // cumulative mass (or count, for top-k) reaches its target bounds, with one bin
-  // of margin each side, a window [lo2, hi2).  The second sums the exact count
-  // and fixed-point mass above hi2 and stages the window's candidates; the exact
-  // descent over them, started from those sums, gives the threshold.  False when
-  // the window misses it or does not fit (the caller then descends the whole row).
+  // (lmax - x) down to fcut (fp32 sums; bin 0 next to the maximum); the bin where
+  // the cumulative mass (or count, for top-k) reaches its target bounds, with
+  // one bin of margin each side, a window [lo2, hi2).  The second sums the exact
+  // count and fixed-point mass above hi2, stages the window's candidates, and
+  // draws Gumbel-max over the candidates above the window (all of them are kept:
+  // the threshold lies in the window) into pre_best / pre_bestv.  The exact
+  // descent over the staged window, started from those sums, gives the
+  // threshold; the draw then adds the window's kept entries.  False when the
+  // window misses the threshold or does not fit (the caller then descends the
+  // whole row, and pre_best is not used).
+  float pre_best = -INFINITY;
+  int pre_bestv = INT_MAX;
   auto window_select = [&](uint32_t& out_key) -> bool {
-    // 16-bit keys need at most two radix passes: the window saves nothing there
-    if (Sp::EB != 4) return false;
     if (!has_p || !(fcut > -INFINITY) || !(lmax > fcut)) return false;
-    const float zspan = (lmax - fcut) / T;                 // scaled width of [fcut, lmax]
-    const float bpl = float(kWinBins) / (zspan * T);       // bins per logit
-    float* wmass = reinterpret_cast<float*>(fsmem);        // [kWarps][kWinBins]
-    unsigned* wcnt = reinterpret_cast<unsigned*>(wmass + kWarps * kWinBins);
-    for (int i = tid; i < kWarps * kWinBins; i += kThreads) {
+    const float bpl = float(kWinBins) / (lmax - fcut);      // bins per logit
+    float* wmass = reinterpret_cast<float*>(fsmem);         // [kWinBins]
+    unsigned* wcnt = reinterpret_cast<unsigned*>(wmass + kWinBins);
+    for (int i = tid; i < kWinBins; i += kThreads) {
       wmass[i] = 0.f;
       wcnt[i] = 0u;
     }
@@ -1489,19 +1595,24 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
       for (int e = 0; e < EPV; ++e) {
         const float x = E::get(raw, e);
         if (!((cb >> e) & 1u) || !(x >= fcut)) continue;
-        const int b = min(max(int((lmax - x) * bpl), 0), kWinBins - 1);
-        atomicAdd(&wmass[warp * kWinBins + b], ex2((x - lmax) * c2));
-        atomicAdd(&wcnt[warp * kWinBins + b], 1u);
+        const int bn = min(max(int((lmax - x) * bpl), 0), kWinBins - 1);
+        atomicAdd(&wmass[bn], ex2((x - lmax) * c2));
+        atomicAdd(&wcnt[bn], 1u);
       }
     });
     __syncthreads();
-    // bin tid (0 = next to the maximum): totals, then an inclusive scan over bins
+    // thread tid sums bins [tid * kWinPer, (tid + 1) * kWinPer); then an
+    // inclusive scan over the threads; the first bin whose cumulative sum
+    // reaches a target is bt
+    constexpr int kWinPer = kWinBins / kThreads;
     double cm = 0.0;  // the bins' sums carry fp32 rounding; the window's margin absorbs it
     unsigned cc = 0u;
-    for (int w = 0; w < kWarps; ++w) {
-      cm += double(wmass[w * kWinBins + tid]);
-      cc += wcnt[w * kWinBins + tid];
+    for (int i = 0; i < kWinPer; ++i) {
+      cm += double(wmass[tid * kWinPer + i]);
+      cc += wcnt[tid * kWinPer + i];
     }
+    const double mine_m = cm;
+    const unsigned mine_c = cc;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const double ym = __shfl_up_sync(kFullWarp, cm, o);
@@ -1524,16 +1635,34 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
       cc += s_wc[w];
     }
     const double target_m = double(fmaxf(rp.tp, 0.f)) * double(S);
-    if (cm >= target_m || (has_k && cc >= unsigned(k))) atomicMin(&s_sel, tid);
+    if (cm >= target_m || (has_k && cc >= unsigned(k))) {
+      // this thread's range reaches a target: find the first bin in it that does
+      double pm = cm - mine_m;
+      unsigned pc = cc - mine_c;
+      int first = kWinPer - 1;
+      for (int i = 0; i < kWinPer; ++i) {
+        pm += double(wmass[tid * kWinPer + i]);
+        pc += wcnt[tid * kWinPer + i];
+        if (pm >= target_m || (has_k && pc >= unsigned(k))) {
+          first = i;
+          break;
+        }
+      }
+      atomicMin(&s_sel, tid * kWinPer + first);
+    }
     __syncthreads();
     const int bt = s_sel;
     if (bt == INT_MAX) return false;
     // the window: bins [bt - 1, bt + 1], as logits
     const float hi2 = bt >= 2 ? __fadd_ru(lmax, -float(bt - 1) / bpl) : INFINITY;
     const float lo2 = fmaxf(__fadd_rd(lmax, -float(bt + 2) / bpl), fcut);
-    // exact count and mass above the window; the window's candidates staged
+    // exact count and mass above the window; the window's candidates staged; the
+    // draw over the candidates above the window (and at or above the min-p cut)
+    const float dcut = fmaxf(hi2, fm);
     unsigned ca = 0u;
     unsigned long long ma = 0ull;
+    uint4 w4 = make_uint4(0, 0, 0, 0);
+    int wgrp = -1;
     if (tid == 0) s_nst = 0u;
     __syncthreads();
     reread([&](const uint4& raw, uint32_t cb, int i0) {
@@ -1544,6 +1673,14 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
         if (cand && x >= hi2) {
           ++ca;
           ma += mass40(x, lmax, c2);
+          if (x >= dcut) {
+            const float z = __fdiv_rn(x, T);
+            if (!(z + kGumbelMax < pre_best)) {
+              const int v = rw.start + i0 + e;
+              const float sc = gumbel_score_vs(z, v, row, a.offset, key, w4, wgrp, pre_best);
+              if (sc > -INFINITY) arg_combine(pre_best, pre_bestv, sc, v);
+            }
+          }
         }
         const bool in = cand && x >= lo2 && x < hi2;
         const unsigned bal = __ballot_sync(kFullWarp, in);
@@ -1578,11 +1715,18 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
     }
     const unsigned nwin = s_nst;
     __syncthreads();
-    if (nwin > unsigned(kStage)) return false;
-    if ((has_k && ca >= unsigned(k)) || ma >= P) return false;  // the threshold is above
+    if (nwin > unsigned(kStage) || (has_k && ca >= unsigned(k)) || ma >= P) {
+      pre_best = -INFINITY;  // the threshold is not in the window: nothing decided
+      pre_bestv = INT_MAX;
+      return false;
+    }
     staged = true;
     nst = nwin;
-    return descend(true, lo2, out_key, hi2, ca, ma);
+    if (descend(true, lo2, out_key, hi2, ca, ma)) return true;
+    staged = false;
+    pre_best = -INFINITY;
+    pre_bestv = INT_MAX;
+    return false;
   };
 
   // At most one staged entry per thread: the threshold by counting.  Thread i
@@ -1769,11 +1913,14 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
       if (!found && !(fm >= lo_b)) from_buffers = false;
     }
     if (!from_buffers) {
-      found = sample_select(kx);
-      if (found)
-        from_buffers = true;  // every kept candidate is staged: the draw takes them
-      else
-        found = window_select(kx) || descend(false, fcut, kx);
+      if (sample_select(kx) || window_select(kx)) {
+        // every kept candidate is staged (the window's, with the ones above it
+        // drawn already into pre_best): the draw takes them
+        found = true;
+        from_buffers = true;
+      } else {
+        found = descend(false, fcut, kx);
+      }
     }
     if (found) thr = fmaxf(key_float(kx), fm);
   } else if (from_buffers && !(fm >= lo_w)) {
@@ -1781,8 +1928,8 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
   }
 
   // ----------------------------------------------------------------- draw
-  float best = -INFINITY;
-  int bestv = INT_MAX;
+  float best = pre_best;  // the window search's draw above its window, if any
+  int bestv = pre_bestv;
   if (from_buffers) {
     buffered([&](float x, int v, bool ok) {
       if (!ok || !(x >= thr)) return;
@@ -1861,8 +2008,12 @@ int elt_bytes(lp_dtype dt) { return dt == LP_F32 ? 4 : 2; }
 // gives kTileTarget tiles (enough for every CTA of the grid to take two), down
 // to the shortest.  It does not depend on the device, so the workspace size can
 // follow it exactly.
+// Float32 tiles are at most 32 KB: a tile's compaction buffer holds 2048
+// float32 entries, and a wide top-p window (top_p 0.99) puts about a sixth of
+// a row's tokens in it.
+int64_t tile_bytes_max(int eb) { return kTileBytesMax; }
 int64_t tile_tokens(int eb, int64_t nrows, int64_t V) {
-  int64_t tile = kTileBytesMax / eb;
+  int64_t tile = tile_bytes_max(eb) / eb;
   while (tile > kTileBytesMin / eb && nrows * std::max<int64_t>(1, (V + tile - 1) / tile) <
                                           kTileTarget)
     tile /= 2;
@@ -1893,7 +2044,7 @@ WsPlan ws_plan(lp_dtype dt, int64_t B, int64_t V) {
   // The bound (and the pool) grow with B and V, so a workspace sized for one
   // shape serves every smaller one.
   const int64_t rows_cap = std::min(B, kMaxRowsPerLaunch);
-  p.tiles = std::max(2 * (kTileTarget - 1), rows_cap * tiles_per_row(kTileBytesMax / eb, V));
+  p.tiles = std::max(2 * (kTileTarget - 1), rows_cap * tiles_per_row(tile_bytes_max(eb) / eb, V));
   p.pool = std::min(std::max(rows_cap * kPoolPerRow, kPoolMin), kPoolMax);
   // The header and the per-row keys must be zero when a call starts; they sit
   // in a region of fixed size at the front, which no call of any shape uses for
