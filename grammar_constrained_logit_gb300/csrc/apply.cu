@@ -47,8 +47,11 @@ struct ApplyArgs {
 __device__ __forceinline__ uint4 ld_stream(const char* p) {
   return __ldcs(reinterpret_cast<const uint4*>(p));
 }
-__device__ __forceinline__ void st_stream(char* p, const uint4& v) {
-  __stcs(reinterpret_cast<uint4*>(p), v);
+// Stores keep the default L2 priority: the masked logits are what the sampler
+// reads next, and evict-first lines would be written back while the next
+// launch's bitmask reads wait on the memory.
+__device__ __forceinline__ void st_vec(char* p, const uint4& v) {
+  *reinterpret_cast<uint4*>(p) = v;
 }
 
 // The fill pattern into the masked elements of one 16-byte vector (bit e of keep
@@ -58,18 +61,18 @@ __device__ __forceinline__ void store_masked(char* p, uint32_t keep, uint32_t fi
   if constexpr (DT == LP_F32) {
 #pragma unroll
     for (int e = 0; e < 4; ++e)
-      if (!((keep >> e) & 1u)) __stcs(reinterpret_cast<unsigned*>(p) + e, fill_w);
+      if (!((keep >> e) & 1u)) *(reinterpret_cast<unsigned*>(p) + e) = fill_w;
   } else {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {  // element pair i is 32-bit word i
       const uint32_t m = (~keep >> (2 * i)) & 3u;
       if (m == 3u)
-        __stcs(reinterpret_cast<unsigned*>(p) + i, fill_w);
+        *(reinterpret_cast<unsigned*>(p) + i) = fill_w;
       else if (m == 1u)
-        __stcs(reinterpret_cast<unsigned short*>(p) + 2 * i, static_cast<unsigned short>(fill_w));
+        *(reinterpret_cast<unsigned short*>(p) + 2 * i) = static_cast<unsigned short>(fill_w);
       else if (m == 2u)
-        __stcs(reinterpret_cast<unsigned short*>(p) + 2 * i + 1,
-               static_cast<unsigned short>(fill_w >> 16));
+        *(reinterpret_cast<unsigned short*>(p) + 2 * i + 1) =
+            static_cast<unsigned short>(fill_w >> 16);
     }
   }
 }
@@ -181,7 +184,7 @@ __global__ void __launch_bounds__(kApplyThreads) apply_kernel(const ApplyArgs a)
         continue;
       }
       const uint4 w = keep[k] == 0u ? fill_v : keep[k] == ALL ? v[k] : E::blend(v[k], keep[k], a.fill);
-      st_stream(dst, w);
+      st_vec(dst, w);
     }
     // block-uniform: the row's first block reports the whole row (its words below
     // vocab_size; an unflagged row keeps every token)
