@@ -11,7 +11,7 @@ One step = one in-place apply over a batch of the first workload plus one fused
 mask + sample over a batch of the second.  Inputs are resident in HBM and rotate
 through rings of copies larger than four L2 caches, so no step reads a batch
 from L2.  Steps are captured in CUDA graphs (launch gaps are those of a graph
-replay; at most K/4 steps per graph, so a run times at least four replays) and
+replay; at most 100 steps per graph, fewer when K is smaller) and
 timed with CUDA events on the launching stream; CUDA events between the apply
 and sample graph replays split the time per kernel.
 
@@ -469,9 +469,13 @@ class Timer:
         """Untimed: a write of twice the L2 evicts every input, then a read of
         another twice the L2 writes those dirty lines back, so that the timed
         kernels neither find their inputs in L2 nor pay for the flush's own
-        write-back."""
+        write-back.  Then the device spins for about 0.25 ms (no memory traffic),
+        so that the host has queued the replay before its start event is
+        recorded: otherwise a run of one or two replays also times the host's
+        submission of its first replay (about 1 us a step on the apply at 20 steps)."""
         self.flush.fill_(r & 0xFF)
         self.sink = self.clean.sum()
+        self.torch.cuda._sleep(500_000)
 
     def run(self, plan, K: int, W: int, G: int, sampler=None):
         torch = self.torch
@@ -511,9 +515,11 @@ class Timer:
 
 
 def graph_len(args) -> int:
-    """Steps per graph: at most --graph-steps, and at most K/4 so that even a short
-    run times at least four replays."""
-    return max(1, min(args.graph_steps, args.steps // 4 if args.steps >= 4 else 1))
+    """Steps per graph: at most --graph-steps and at most K.  A graph's replay
+    costs a few microseconds before its first kernel starts; the longer the graph,
+    the less of that lands on each step (the inputs rotate through rings larger
+    than the L2, so a long graph reads none of them from L2)."""
+    return max(1, min(args.graph_steps, args.steps))
 
 
 def op_line(op, sec: float, ws: int, peak: dict) -> dict:
