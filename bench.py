@@ -11,7 +11,8 @@ One step = one in-place apply over a batch of the first workload plus one fused
 mask + sample over a batch of the second.  Inputs are resident in HBM and rotate
 through rings of copies larger than four L2 caches, so no step reads a batch
 from L2.  Steps are captured in CUDA graphs (launch gaps are those of a graph
-replay; at most 100 steps per graph, fewer when K is smaller) and
+replay; at most 100 steps per graph and at most K/4, so a run times at least
+four replays) and
 timed with CUDA events on the launching stream; CUDA events between the apply
 and sample graph replays split the time per kernel.
 
@@ -515,11 +516,12 @@ class Timer:
 
 
 def graph_len(args) -> int:
-    """Steps per graph: at most --graph-steps and at most K.  A graph's replay
-    costs a few microseconds before its first kernel starts; the longer the graph,
-    the less of that lands on each step (the inputs rotate through rings larger
-    than the L2, so a long graph reads none of them from L2)."""
-    return max(1, min(args.graph_steps, args.steps))
+    """Steps per graph: at most --graph-steps, and at most K/4 so that even a short
+    run times at least four replays.  Each replay starts after the L2 has been
+    emptied, with the kernels' code and parameters cold as well, which costs
+    5-7 us once per replay: a 20-step run (graphs of 5) carries about 1 us of it
+    per step, a 2000-step run (graphs of 100) almost none."""
+    return max(1, min(args.graph_steps, args.steps // 4 if args.steps >= 4 else 1))
 
 
 def op_line(op, sec: float, ws: int, peak: dict) -> dict:
