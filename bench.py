@@ -35,7 +35,6 @@ reference arm.
 from __future__ import annotations
 
 import argparse
-import glob
 import hashlib
 import json
 import os
@@ -210,28 +209,37 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
-def kernel_source_hash() -> str:
+# the sources each kernel is compiled from (with include/lp.h)
+KERNEL_SOURCES = {
+    "apply_kernel": ("apply.cu", "common.cuh"),
+    "sample_stream_kernel": ("sample.cu", "common.cuh"),
+    "sample_finish_kernel": ("sample.cu", "common.cuh"),
+}
+
+
+def kernel_source_hash(kernel: str, read=None) -> str:
+    """Hash of the sources `kernel` is built from; `read(path)` gives a file's bytes
+    (default: the working tree)."""
+    read = read or (lambda rel: open(os.path.join(ROOT, rel), "rb").read())
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "grammar_constrained_logit_gb300", "csrc", "*"))):
-        h.update(open(f, "rb").read())
-    h.update(open(os.path.join(ROOT, "include", "lp.h"), "rb").read())
+    for f in KERNEL_SOURCES[kernel]:
+        h.update(read(os.path.join("grammar_constrained_logit_gb300", "csrc", f)))
+    h.update(read(os.path.join("include", "lp.h")))
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernels, workload: str):
     """DRAM bytes per launch of the given kernels (summed: one hot-path call), from
-    the committed ncu captures, if they were taken on the current kernel sources;
-    else None."""
+    the committed ncu captures, if each was taken on its kernel's current
+    sources; else None."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
-    if d.get("source_hash") != kernel_source_hash():
-        return None
     total = 0
     for k in ([kernels] if isinstance(kernels, str) else kernels):
         e = d.get("kernels", {}).get(f"{k}:{workload}")
-        if e is None:
+        if e is None or e.get("source_hash") != kernel_source_hash(k):
             return None
         total += int(e["dram_bytes_per_launch"])
     return total
@@ -527,7 +535,7 @@ def graph_len(args) -> int:
 def op_line(op, sec: float, ws: int, peak: dict) -> dict:
     """One op's figures: time per launch, throughput and its roofline (dense and
     sector-minimal bytes)."""
-    wl = op.w.name
+    wl = op.w.name + ("_rows" if op.kind == "apply" and op.flags is not None else "")
     knames = (["apply_kernel"] if op.kind == "apply" else
               ["sample_stream_kernel", "sample_finish_kernel"])
     rf = roofline(op.bytes, sec, peak, ncu_traffic(knames, wl), op.sector_minimal)

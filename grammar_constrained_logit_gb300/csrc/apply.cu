@@ -24,6 +24,7 @@ namespace {
 constexpr int kApplyThreads = 256;
 constexpr int kVecPerThread = 4;
 constexpr int kVecPerBlock = kApplyThreads * kVecPerThread;
+constexpr int kReportBatch = 4;  // mask words a thread loads at once for the report
 
 struct ApplyArgs {
   char* out;                  // out of place: destination rows
@@ -187,15 +188,27 @@ __global__ void __launch_bounds__(kApplyThreads) apply_kernel(const ApplyArgs a)
       st_vec(dst, w);
     }
     // block-uniform: the row's first block reports the whole row (its words below
-    // vocab_size; an unflagged row keeps every token)
+    // vocab_size; an unflagged row keeps every token).  The mask bits of its own
+    // vectors, already loaded, settle most flagged rows; the others read every
+    // word of the row, kReportBatch independent loads a thread at a time.
     if (!OOP && a.has_token != nullptr && blockIdx.x == 0) {
       bool kept = !sel && a.vocab > 0;
       if (sel) {
+#pragma unroll
+        for (int k = 0; k < kVecPerThread; ++k) kept |= keep[k] != ~0u && keep[k] != 0u;
+      }
+      if (sel && !__syncthreads_or(kept)) {
         const int64_t nw = (a.vocab + 31) >> 5;
-        for (int64_t w = threadIdx.x; w < nw; w += blockDim.x) {
-          uint32_t word = __ldg(mrow + w);
-          if (w == nw - 1 && (a.vocab & 31)) word &= (1u << (a.vocab & 31)) - 1u;
-          kept |= word != 0u;
+        const uint32_t last = (a.vocab & 31) ? (1u << (a.vocab & 31)) - 1u : ~0u;
+        for (int64_t w0 = threadIdx.x; w0 < nw; w0 += int64_t(kReportBatch) * blockDim.x) {
+          uint32_t wd[kReportBatch];
+#pragma unroll
+          for (int u = 0; u < kReportBatch; ++u) {
+            const int64_t w = w0 + int64_t(u) * blockDim.x;
+            wd[u] = w < nw ? __ldg(mrow + w) & (w == nw - 1 ? last : ~0u) : 0u;
+          }
+#pragma unroll
+          for (int u = 0; u < kReportBatch; ++u) kept |= wd[u] != 0u;
         }
       }
       const int r = __syncthreads_or(kept);

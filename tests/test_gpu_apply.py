@@ -185,6 +185,38 @@ def test_rows_parity(dtype):
         assert bm_rows >= B
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_rows_report_single_token_anywhere(dtype):
+    """Flagged rows that keep exactly one token: in the ragged head before the
+    first 16-byte boundary, past the first block's tokens, in the last partial
+    word below vocab_size, just above vocab_size (not kept), or none at all; the
+    report and the logits match the oracle bit for bit."""
+    rng = np.random.default_rng(4100 + DT[dtype])
+    B, V = 48, 40007
+    words = (V + 31) // 32
+    vocab = V - 5
+    logits = syn.to_storage(rng.standard_normal((B, V)).astype(np.float32), dtype)
+    allowed = np.zeros((B, words * 32), dtype=bool)
+    spots = [0, 1, 2, 3, 7, 9000, 20000, 33000, vocab - 1, vocab - 2, vocab, V - 1]
+    for r in range(B):
+        if r % 8 == 7:
+            continue  # no token at all
+        allowed[r, spots[r % len(spots)] if r < 24 else int(rng.integers(0, V))] = True
+    bm = syn.pack_bits(allowed)
+    flags = np.ones(B, dtype=np.uint8)
+    flags[5] = 0
+    guard, shift = 64, 1
+    base, view = _dev_view(logits, dtype, guard, shift)
+    want, want_has = oracle.apply_rows(logits, bm, dtype=DT[dtype], flags=flags,
+                                       vocab_size=vocab, cols=V)
+    has = ops.apply_token_bitmask_rows(view[:, :V], torch.from_numpy(bm).cuda(),
+                                       torch.from_numpy(flags).cuda(), vocab_size=vocab,
+                                       report=True)
+    assert np.array_equal(_bits(_host(view, dtype)), _bits(want))
+    assert has.cpu().numpy().tolist() == want_has.tolist()
+    _check_guard(base, dtype, guard, shift, B * logits.shape[1])
+
+
 def test_rows_report_overwrites_and_without_report():
     x = torch.zeros(3, 100, device="cuda")
     bm = torch.zeros(3, 4, dtype=torch.int32, device="cuda")

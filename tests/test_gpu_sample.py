@@ -274,6 +274,36 @@ def test_filter_grid_parity(dtype):
     pool.done()
 
 
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_small_top_k_rows_parity(dtype):
+    """Top-k rows with k <= 32 and around it: Gaussian rows, rows of a few
+    repeated values (ties at the k-th logit), rows with fewer candidates than k,
+    and rows whose candidates sit in one short run of the vocabulary."""
+    rng = np.random.default_rng(91 + DT[dtype])
+    B, V = 96, 40000
+    x = rng.standard_normal((B, V)).astype(np.float32) * np.float32(2.0)
+    x[1::4] = np.round(x[1::4])                      # ties
+    st = syn.to_storage(x, dtype)
+    allowed = rng.random((B, V)) < 0.6
+    allowed[2::4] = False                            # a handful of candidates
+    for r in range(2, B, 4):
+        allowed[r, rng.choice(V, size=int(rng.integers(1, 40)), replace=False)] = True
+    allowed[3::4] = False                            # one short run
+    for r in range(3, B, 4):
+        s0 = int(rng.integers(0, V - 3000))
+        allowed[r, s0:s0 + 3000] = True
+    w = syn.Workload("topk", dtype, st, V, V, bitmask=syn.pack_bits(allowed), seed=6)
+    ks = np.array([1, 2, 7, 20, 31, 32, 33, 50], np.int32)
+    w.temperature = rng.uniform(0.4, 1.6, B).astype(np.float32)
+    w.top_k = ks[np.arange(B) % len(ks)]
+    w.top_p = np.where(np.arange(B) % 3 == 0, 0.9, 1.0).astype(np.float32)
+    w.min_p = np.where(np.arange(B) % 5 == 0, 0.05, 0.0).astype(np.float32)
+    pool = Pool(f"top-k rows with k near 32, {dtype} (ties, few candidates, one run)")
+    for off in range(53):
+        pool.add(check_rows(w, off, run_gpu(w, off)))
+    pool.done()
+
+
 def test_masked_token_never_drawn_and_indices():
     rng = np.random.default_rng(8)
     B, V = 64, 4099
