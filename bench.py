@@ -364,90 +364,132 @@ class Op:
         return g
 
 
-def e2e_apply(w: syn.Workload, steps: int, torch, ops) -> dict:
-    """apply_token_bitmask_inplace through the public API, inputs from pinned
-    host memory and the result copied back, per step."""
-    dev = torch.device("cuda")
+class E2EPipeline:
+    """Steps through the public API with host inputs and a host result, the way a
+    serving loop overlaps them: step i's upload (pinned host to device, on its own
+    stream) runs while step i - 1 is applied and read back; two sets of device
+    buffers alternate.  Every step still copies all of its inputs in and its
+    result out inside the timed region."""
+
+    def __init__(self, torch, make_set):
+        self.torch = torch
+        self.sets = [make_set(), make_set()]
+        self.up, self.work = torch.cuda.Stream(), torch.cuda.Stream()
+        self.ready = [torch.cuda.Event(), torch.cuda.Event()]
+        self.free = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def step(self, i, upload, run):
+        k = i % 2
+        b = self.sets[k]
+        with self.torch.cuda.stream(self.up):
+            self.up.wait_event(self.free[k])  # the set's previous result is read back
+            upload(b)
+            self.ready[k].record(self.up)
+        with self.torch.cuda.stream(self.work):
+            self.work.wait_event(self.ready[k])
+            run(b, i)
+            self.free[k].record(self.work)
+
+    def time(self, steps, upload, run) -> float:
+        torch = self.torch
+        for i in range(3):
+            self.step(i, upload, run)
+        torch.cuda.synchronize()
+        cur = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(cur)
+        self.up.wait_stream(cur)
+        self.work.wait_stream(cur)
+        for i in range(steps):
+            self.step(i, upload, run)
+        cur.wait_stream(self.up)
+        cur.wait_stream(self.work)
+        e1.record(cur)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / steps
+
+
+def _pinned_logits(w: syn.Workload, torch):
     if w.dtype == "bf16":
-        host = torch.from_numpy(w.logits.view(np.int16)).view(torch.bfloat16).pin_memory()
-    else:
-        host = torch.from_numpy(w.logits).pin_memory()
+        return torch.from_numpy(w.logits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    return torch.from_numpy(w.logits).pin_memory()
+
+
+def e2e_apply(w: syn.Workload, steps: int, torch, ops) -> dict:
+    """apply_token_bitmask_inplace through the public API: per step the logits,
+    bitmask and indices copied in from pinned host memory, the masked logits
+    copied back (consecutive steps overlap, E2EPipeline)."""
+    dev = torch.device("cuda")
+    host = _pinned_logits(w, torch)
     bm_h = torch.from_numpy(w.bitmask).pin_memory()
     idx_h = None if w.indices is None else torch.from_numpy(w.indices).pin_memory()
     out_h = torch.empty_like(host).pin_memory()
-    lg = torch.empty_like(host, device=dev)
-    bm = torch.empty_like(bm_h, device=dev)
-    idx = None if idx_h is None else torch.empty_like(idx_h, device=dev)
 
-    def step():
-        lg.copy_(host, non_blocking=True)
-        bm.copy_(bm_h, non_blocking=True)
-        if idx is not None:
-            idx.copy_(idx_h, non_blocking=True)
-        ops.apply_token_bitmask_inplace(lg[:, :w.cols], bm, vocab_size=w.vocab_size, indices=idx)
-        out_h.copy_(lg, non_blocking=True)
+    def make_set():
+        return {"lg": torch.empty_like(host, device=dev), "bm": torch.empty_like(bm_h, device=dev),
+                "idx": None if idx_h is None else torch.empty_like(idx_h, device=dev)}
 
-    for _ in range(3):
-        step()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
-        step()
-    e1.record()
-    torch.cuda.synchronize()
-    sec = e0.elapsed_time(e1) / 1e3 / steps
+    def upload(b):
+        b["lg"].copy_(host, non_blocking=True)
+        b["bm"].copy_(bm_h, non_blocking=True)
+        if idx_h is not None:
+            b["idx"].copy_(idx_h, non_blocking=True)
+
+    def run(b, i):
+        ops.apply_token_bitmask_inplace(b["lg"][:, :w.cols], b["bm"], vocab_size=w.vocab_size,
+                                        indices=b["idx"])
+        out_h.copy_(b["lg"], non_blocking=True)
+
+    sec = E2EPipeline(torch, make_set).time(steps, upload, run)
     h2d = host.numel() * host.element_size() + bm_h.numel() * 4 + (0 if idx_h is None else idx_h.numel() * 4)
     return {"value": round(apply_bytes(w) / sec / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(out_h.numel() * out_h.element_size()),
-            "ms_per_step": round(sec * 1e3, 4)}
+            "ms_per_step": round(sec * 1e3, 4),
+            "copies": "every step's inputs in and result out; step i's upload overlaps step i-1's apply and read-back"}
 
 
 def e2e_sample(w: syn.Workload, steps: int, torch, ops) -> dict:
+    """mask_and_sample through the public API: per step the logits, bitmask,
+    indices and parameters copied in from pinned host memory, the ids copied
+    back (consecutive steps overlap, E2EPipeline)."""
     dev = torch.device("cuda")
-    if w.dtype == "bf16":
-        host = torch.from_numpy(w.logits.view(np.int16)).view(torch.bfloat16).pin_memory()
-    else:
-        host = torch.from_numpy(w.logits).pin_memory()
+    host = _pinned_logits(w, torch)
     bm_h = None if w.bitmask is None else torch.from_numpy(w.bitmask).pin_memory()
     idx_h = None if w.indices is None else torch.from_numpy(w.indices).pin_memory()
     par_h = {k: torch.from_numpy(w.per_row(k)).pin_memory()
              for k in ("temperature", "top_k", "top_p", "min_p")}
-    lg = torch.empty_like(host, device=dev)
-    bm = None if bm_h is None else torch.empty_like(bm_h, device=dev)
-    idx = None if idx_h is None else torch.empty_like(idx_h, device=dev)
-    par = {k: torch.empty_like(v, device=dev) for k, v in par_h.items()}
-    ids = torch.empty(w.B, dtype=torch.int64, device=dev)
     ids_h = torch.empty(w.B, dtype=torch.int64).pin_memory()
 
-    def step(i):
-        lg.copy_(host, non_blocking=True)
-        if bm is not None:
-            bm.copy_(bm_h, non_blocking=True)
-        if idx is not None:
-            idx.copy_(idx_h, non_blocking=True)
-        for k in par:
-            par[k].copy_(par_h[k], non_blocking=True)
-        ops.mask_and_sample(lg[:, :w.cols], bm, par["temperature"], par["top_k"], par["top_p"],
-                            par["min_p"], seed=w.seed, offset=w.offsets[i % len(w.offsets)],
-                            indices=idx, vocab_size=w.vocab_size if bm is not None else None,
-                            out=ids)
-        ids_h.copy_(ids, non_blocking=True)
+    def make_set():
+        return {"lg": torch.empty_like(host, device=dev),
+                "bm": None if bm_h is None else torch.empty_like(bm_h, device=dev),
+                "idx": None if idx_h is None else torch.empty_like(idx_h, device=dev),
+                "par": {k: torch.empty_like(v, device=dev) for k, v in par_h.items()},
+                "ids": torch.empty(w.B, dtype=torch.int64, device=dev)}
 
-    for i in range(3):
-        step(i)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for i in range(steps):
-        step(i)
-    e1.record()
-    torch.cuda.synchronize()
-    sec = e0.elapsed_time(e1) / 1e3 / steps
+    def upload(b):
+        b["lg"].copy_(host, non_blocking=True)
+        if bm_h is not None:
+            b["bm"].copy_(bm_h, non_blocking=True)
+        if idx_h is not None:
+            b["idx"].copy_(idx_h, non_blocking=True)
+        for k in par_h:
+            b["par"][k].copy_(par_h[k], non_blocking=True)
+
+    def run(b, i):
+        p = b["par"]
+        ops.mask_and_sample(b["lg"][:, :w.cols], b["bm"], p["temperature"], p["top_k"], p["top_p"],
+                            p["min_p"], seed=w.seed, offset=w.offsets[i % len(w.offsets)],
+                            indices=b["idx"], vocab_size=w.vocab_size if bm_h is not None else None,
+                            out=b["ids"])
+        ids_h.copy_(b["ids"], non_blocking=True)
+
+    sec = E2EPipeline(torch, make_set).time(steps, upload, run)
     h2d = host.numel() * host.element_size() + (0 if bm_h is None else bm_h.numel() * 4) + \
         (0 if idx_h is None else idx_h.numel() * 4) + sum(v.numel() * 4 for v in par_h.values())
     return {"value": round(w.B / sec, 1), "unit": "rows/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(8 * w.B), "ms_per_step": round(sec * 1e3, 4)}
+            "d2h_bytes_per_step": int(8 * w.B), "ms_per_step": round(sec * 1e3, 4),
+            "copies": "every step's inputs in and ids out; step i's upload overlaps step i-1's sampling"}
 
 
 def roofline(bytes_per_launch: int, sec_per_launch: float, peak: dict, traffic,
