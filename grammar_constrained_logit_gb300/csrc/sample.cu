@@ -1357,6 +1357,35 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
     }
   };
 
+  // Stages the elements of vector `raw` whose bits are set in `inb` (element e is
+  // token tok0 + e) at consecutive places of the stage, taken for the whole warp
+  // with one shared-memory atomic: a per-lane count, a scan over the lanes, and
+  // stores at fixed element indices.  Warp-uniform.  The order of staged entries
+  // is immaterial (the selections count, the draw breaks ties by token).
+  auto stage_vec = [&](const uint4& raw, uint32_t inb, int tok0) {
+    const int c = __popc(inb);
+    if (!__any_sync(kFullWarp, c != 0)) return;
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFullWarp, incl, o);
+      if (lane >= o) incl += y;
+    }
+    unsigned base = 0u;
+    if (lane == 31) base = atomicAdd(&s_nst, unsigned(incl));
+    unsigned pos = __shfl_sync(kFullWarp, base, 31) + unsigned(incl - c);
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) {
+      if ((inb >> e) & 1u) {
+        if (pos < unsigned(kStage)) {
+          bval[pos] = E::get(raw, e);
+          bidx[pos] = tok0 + e;
+        }
+        ++pos;
+      }
+    }
+  };
+
   // ---------------------------------- radix select of the threshold
   const unsigned long long P = bd.P;  // fixed-point top-p mass target
   // a radix pass keeps its bins' masses in 32-bit limbs unless the row has more
@@ -1666,6 +1695,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
     if (tid == 0) s_nst = 0u;
     __syncthreads();
     reread([&](const uint4& raw, uint32_t cb, int i0) {
+      uint32_t inb = 0u;
 #pragma unroll
       for (int e = 0; e < EPV; ++e) {
         const float x = E::get(raw, e);
@@ -1682,19 +1712,9 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
             }
           }
         }
-        const bool in = cand && x >= lo2 && x < hi2;
-        const unsigned bal = __ballot_sync(kFullWarp, in);
-        unsigned base = 0u;
-        if (lane == 0 && bal) base = atomicAdd(&s_nst, unsigned(__popc(bal)));
-        base = __shfl_sync(kFullWarp, base, 0);
-        if (in) {
-          const unsigned pos = base + unsigned(__popc(bal & ((1u << lane) - 1u)));
-          if (pos < unsigned(kStage)) {
-            bval[pos] = x;
-            bidx[pos] = rw.start + i0 + e;
-          }
-        }
+        if (cand && x >= lo2 && x < hi2) inb |= 1u << e;
       }
+      stage_vec(raw, inb, rw.start + i0);
     });
     // block sums of the exact counts above the window
 #pragma unroll
@@ -1794,19 +1814,13 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
         cb = rw.bits(q, i0, nullptr, 0, 0);
         if (cb) raw = rw.gvec(q);
       }
+      uint32_t inb = 0u;
 #pragma unroll
       for (int e = 0; e < EPV; ++e) {
         const float x = E::get(raw, e);
-        const bool in = ((cb >> e) & 1u) && x > -INFINITY && x >= fcut;
-        const unsigned bal = __ballot_sync(kFullWarp, in);
-        unsigned pos = 0u;
-        if (lane == 0 && bal) pos = atomicAdd(&s_nst, unsigned(__popc(bal)));
-        pos = __shfl_sync(kFullWarp, pos, 0) + unsigned(__popc(bal & ((1u << lane) - 1u)));
-        if (in && pos < unsigned(kStage)) {
-          bval[pos] = x;
-          bidx[pos] = rw.start + i0 + e;
-        }
+        if (((cb >> e) & 1u) && x > -INFINITY && x >= fcut) inb |= 1u << e;
       }
+      stage_vec(raw, inb, rw.start + i0);
     }
     __syncthreads();
     nst = min(s_nst, unsigned(kStage));
@@ -1856,24 +1870,17 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
     if (tid == 0) s_nst = 0u;
     __syncthreads();
     reread([&](const uint4& raw, uint32_t cb, int i0) {
+      uint32_t inb = 0u;
 #pragma unroll
       for (int e = 0; e < EPV; ++e) {
         const float x = E::get(raw, e);
-        const bool in = ((cb >> e) & 1u) && x > -INFINITY && x >= bnd;
-        if (in) {
+        if (((cb >> e) & 1u) && x > -INFINITY && x >= bnd) {
+          inb |= 1u << e;
           ++ca;
           if (has_p) ma += mass40(x, lmax, c2);
         }
-        const unsigned bal = __ballot_sync(kFullWarp, in);
-        if (!bal) continue;
-        unsigned pos = 0u;
-        if (lane == 0) pos = atomicAdd(&s_nst, unsigned(__popc(bal)));
-        pos = __shfl_sync(kFullWarp, pos, 0) + unsigned(__popc(bal & ((1u << lane) - 1u)));
-        if (in && pos < unsigned(kStage)) {
-          bval[pos] = x;
-          bidx[pos] = rw.start + i0 + e;
-        }
       }
+      stage_vec(raw, inb, rw.start + i0);
     });
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
