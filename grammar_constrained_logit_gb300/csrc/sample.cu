@@ -259,6 +259,33 @@ __device__ __forceinline__ float gumbel_score_vs(float z, int v, int row, uint64
   return z + gumbel_from_word(word);
 }
 
+// x * (1 / T) is within 3 * 2^-24 relative of x / T; a bound widened by 2^-20 of
+// |z| therefore holds for either.
+constexpr float kZRel = 9.5367431640625e-07f;  // 2^-20
+
+// gumbel_score_vs for logit x, with z = x / T formed only for a token that the
+// skip test lets through: the test takes x * invT and a bound widened by kZRel,
+// so a skipped token still provably cannot reach `best`, and the score of a
+// token that is not skipped is the one gumbel_score_vs gives.
+__device__ __forceinline__ float gumbel_score_vx(float x, float T, float invT, int v, int row,
+                                                uint64_t offset, uint2 key, uint4& w4, int& wgrp,
+                                                float best) {
+  const int grp = v >> 2;
+  if (grp != wgrp) {
+    w4 = philox4x32_10(
+        make_uint4(uint32_t(grp), uint32_t(row), uint32_t(offset), uint32_t(offset >> 32)), key);
+    wgrp = grp;
+  }
+  const uint32_t word = (v & 3) == 0 ? w4.x : (v & 3) == 1 ? w4.y : (v & 3) == 2 ? w4.z : w4.w;
+  if (best > -INFINITY) {
+    const float za = x * invT;
+    const float one_minus_u = (float(8388608u - (word >> 9)) - 0.5f) * 1.1920928955078125e-07f;
+    const float bound = ex2((za - best + fabsf(za) * kZRel) * kLog2e) * 1.0001f;
+    if (one_minus_u > bound) return -INFINITY;
+  }
+  return __fdiv_rn(x, T) + gumbel_from_word(word);
+}
+
 // Programmatic dependent launch: wait for the grid this one depends on, and let
 // the next grid in the stream begin its launch.
 __device__ __forceinline__ void grid_dependency_wait() {
@@ -1099,6 +1126,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
   const uint2 key = philox_key(a, row);
   const RowParams rp = row_params(raw_params(a, row));
   const float T = rp.T, c2 = rp.c2;
+  const float invT = 1.f / T;  // for skip tests only (scores divide by T)
   const bool has_p = rp.has_p;
   const int64_t t0 = int64_t(lrow) * a.tpr;
   const TileSum* rts = a.ts + t0;
@@ -1704,10 +1732,11 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
           ++ca;
           ma += mass40(x, lmax, c2);
           if (x >= dcut) {
-            const float z = __fdiv_rn(x, T);
-            if (!(z + kGumbelMax < pre_best)) {
+            const float za = x * invT;  // the tests' stand-in for x / T
+            if (!(za + fabsf(za) * kZRel + kGumbelMax < pre_best)) {
               const int v = rw.start + i0 + e;
-              const float sc = gumbel_score_vs(z, v, row, a.offset, key, w4, wgrp, pre_best);
+              const float sc =
+                  gumbel_score_vx(x, T, invT, v, row, a.offset, key, w4, wgrp, pre_best);
               if (sc > -INFINITY) arg_combine(pre_best, pre_bestv, sc, v);
             }
           }
@@ -1952,11 +1981,11 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
       for (int e = 0; e < EPV; ++e) {
         const float x = E::get(raw, e);
         if (!((cb >> e) & 1u) || !(x >= thr) || !(x > -INFINITY)) continue;
-        const float z = __fdiv_rn(x, T);
-        if (z + kGumbelMax < best) continue;
+        const float za = x * invT;  // the tests' stand-in for x / T
+        if (za + fabsf(za) * kZRel + kGumbelMax < best) continue;
         const int v = rw.start + i0 + e;
-        arg_combine(best, bestv, gumbel_score_vs(z, v, row, a.offset, key, w4, wgrp, best),
-                    v);
+        arg_combine(best, bestv,
+                    gumbel_score_vx(x, T, invT, v, row, a.offset, key, w4, wgrp, best), v);
       }
     });
   }
