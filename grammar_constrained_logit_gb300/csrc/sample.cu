@@ -1135,8 +1135,55 @@ __global__ void __launch_bounds__(kThreads, 4) sample_finish_kernel(const Sample
   // ------------------------------------------- merge the tile summaries
   // Thread tid takes a contiguous run of tiles in order, then a fixed tree over
   // the threads: a deterministic merge.  Buffered entries per tile are counted
-  // for the staging below.
-  {
+  // for the staging below.  A row of at most 32 tiles is merged by warp 0 alone,
+  // one tile a lane, by the same tree (the other warps would hold only
+  // identities, whose merge changes nothing).
+  if (a.tpr <= 32) {
+    if (warp == 0) {
+      float wm = -INFINITY, ws = 0.f, wb = -INFINITY;
+      int wv = INT_MAX, wn = 0, wbv = INT_MAX;
+      unsigned flags = 0u, nbuf = 0u;
+      if (lane < a.tpr) {
+        const TileSum st = rts[lane];
+        wn = st.ncand;
+        row_combine(wm, wv, ws, st.max, st.arg, st.sum, c2, has_p);
+        arg_combine(wb, wbv, st.best, st.best_v);
+        flags = st.nf & (kTileOverflow | kTileError);
+        nbuf = (st.nf & (kTileOverflow | kTileError)) ? 0u : st.nf;
+      }
+      unsigned incl = nbuf;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(kFullWarp, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (meta && lane < a.tpr) tstart[lane] = incl - nbuf;  // the tile's start
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const float m2 = __shfl_xor_sync(kFullWarp, wm, o);
+        const float s2 = __shfl_xor_sync(kFullWarp, ws, o);
+        const int v2 = __shfl_xor_sync(kFullWarp, wv, o);
+        wn += __shfl_xor_sync(kFullWarp, wn, o);
+        row_combine(wm, wv, ws, m2, v2, s2, c2, has_p);
+        const float b2 = __shfl_xor_sync(kFullWarp, wb, o);
+        const int bv2 = __shfl_xor_sync(kFullWarp, wbv, o);
+        arg_combine(wb, wbv, b2, bv2);
+        flags |= __shfl_xor_sync(kFullWarp, flags, o);
+      }
+      const unsigned tot = __shfl_sync(kFullWarp, incl, 31);
+      if (lane == 0) {
+        s_f[0] = wm;
+        s_f[1] = ws;
+        s_i[0] = wv;
+        s_i[1] = wn;
+        s_i[2] = wbv;
+        s_i[3] = int(flags >> 30);  // bit 0 overflow, bit 1 error
+        s_total = tot;
+        if (meta) tstart[a.tpr] = tot;
+      }
+    }
+    __syncthreads();
+  } else {
     const int per = (a.tpr + kThreads - 1) / kThreads;
     const int tb = min(tid * per, a.tpr), te = min(tb + per, a.tpr);
     float wm = -INFINITY, ws = 0.f, wb = -INFINITY;
